@@ -1,0 +1,22 @@
+"""Seeded synthetic workloads for DCP decode attention.
+
+This module is shared by the CUDA path's tests/bench and by the oracle's tests.
+It holds no arithmetic of the method itself: it only draws random numbers,
+rounds them to the storage dtype with library casts, lays tokens out densely
+per request, and hands out physical block ids from a random permutation once a
+caller has said how many blocks each (rank, request) needs.
+"""
+
+from .configs import CONFIGS, CONFIG_ORDER, config
+from .gen import Workload, make_workload, allocate_blocks, bf16_bits, fp8_bits
+
+__all__ = [
+    "CONFIGS",
+    "CONFIG_ORDER",
+    "config",
+    "Workload",
+    "make_workload",
+    "allocate_blocks",
+    "bf16_bits",
+    "fp8_bits",
+]

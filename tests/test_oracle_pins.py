@@ -1,0 +1,339 @@
+"""Pins for the CPU oracle: values the pages print, closed forms, invariants,
+and special cases that reduce to a library routine (torch SDPA in fp64).
+
+Each check is chosen so that a plausible slip in the oracle (a wrong index,
+a dropped max shift, a transposed operand, a wrong head mapping or causal
+bound, a wrong merge weight) fails at least one of them.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dcp_workloads import allocate_blocks, config, make_workload
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read(name):
+    lines = []
+    for ln in open(os.path.join(GOLDEN, name)):
+        ln = ln.split("#")[0].strip()
+        if ln:
+            lines.append(ln)
+    return lines
+
+
+# ---------------------------------------------------------------- ownership
+
+def test_worked_interleave_table():
+    lines = _read("interleave_I4_N4.txt")
+    N = int(lines[0].split()[1])
+    I = int(lines[1].split()[1])
+    for ln in lines[2:]:
+        a, b, r = map(int, ln.split())
+        for t in range(a, b + 1):
+            assert oracle.rank_of(t, N, I) == r, (t, r)
+
+
+def test_contiguous_ranges_are_interleave_with_large_I():
+    lines = _read("contiguous_ranges.txt")
+    L = int(lines[0].split()[1])
+    N = int(lines[1].split()[1])
+    I = int(lines[2].split()[1])
+    rank, _ = oracle.local_layout(L, N, I)
+    for ln in lines[3:]:
+        a, b, r = map(int, ln.split())
+        assert np.all(rank[a:b + 1] == r)
+    for r in range(N):
+        assert oracle.local_len(L, r, N, I) == L // N
+
+
+@pytest.mark.parametrize("N,I", [(1, 1), (2, 1), (3, 2), (4, 4), (8, 1), (8, 64), (5, 3)])
+def test_ownership_period(N, I):
+    # ownership repeats every N x I tokens ("vLLM DCP and PCP", TL;DR)
+    for t in range(0, 3 * N * I + 7):
+        assert oracle.rank_of(t + N * I, N, I) == oracle.rank_of(t, N, I)
+    # and within one period every rank owns exactly I consecutive tokens
+    rank, _ = oracle.local_layout(N * I, N, I)
+    assert np.all(np.bincount(rank, minlength=N) == I)
+
+
+# ------------------------------------------------------------ local lengths
+
+def test_even_split_8k_on_4():
+    for ln in _read("even_split.txt"):
+        L, N, I, each = map(int, ln.split())
+        assert [oracle.local_len(L, r, N, I) for r in range(N)] == [each] * N
+
+
+@pytest.mark.parametrize("N,I", [(2, 1), (4, 2), (4, 4), (3, 5), (8, 1), (8, 64), (4, 16)])
+def test_local_lengths_partition_and_spread(N, I):
+    rng = np.random.default_rng(7)
+    for L in list(range(0, 3 * N * I + 3)) + list(rng.integers(1, 5000, size=20)):
+        lens = [oracle.local_len(int(L), r, N, I) for r in range(N)]
+        assert sum(lens) == L
+        # "local sequence lengths can differ by at most one interleave group"
+        assert max(lens) - min(lens) <= I
+        # lower ranks never hold fewer tokens than higher ranks
+        assert all(lens[r] >= lens[r + 1] for r in range(N - 1))
+
+
+@pytest.mark.parametrize("N,I", [(2, 1), (4, 2), (3, 5), (8, 64)])
+def test_local_positions_form_a_prefix(N, I):
+    # each rank's tokens among the first L occupy local positions 0..len-1 in order
+    L = 4 * N * I + 3
+    rank, lpos = oracle.local_layout(L, N, I)
+    for Lp in range(L + 1):
+        for r in range(N):
+            mine = lpos[:Lp][rank[:Lp] == r]
+            assert np.array_equal(mine, np.arange(oracle.local_len(Lp, r, N, I)))
+
+
+def test_pd_block_fill_example():
+    lines = _read("pd_block_fill.txt")
+    L = int(lines[0].split()[1])
+    bs = int(lines[1].split()[1])
+    N = int(lines[2].split()[1])
+    for ln in lines[3:]:
+        head, blocks, virt = ln.split("|")
+        head = list(map(int, head.split()))
+        I, lens = head[0], head[1:]
+        sm = oracle.slot_mapping(N, I, bs, np.array([L]), np.zeros(L, np.int32), np.arange(L))
+        assert sm["local_lens"][:, 0].tolist() == lens
+        assert sm["rank_blocks"][:, 0].tolist() == list(map(int, blocks.split()))
+        assert sm["virt_blocks"].tolist() == [int(virt)]
+        # fill ratio of each non-empty block: 25% at I=1, 100% at I=bs
+        fill = [n / (math.ceil(n / bs) * bs) for n in lens if n]
+        assert fill == ([0.25] * 4 if I == 1 else [1.0])
+
+
+@pytest.mark.parametrize("N,I,bs", [(4, 1, 16), (4, 4, 16), (8, 64, 64), (2, 8, 16), (8, 1, 64)])
+def test_rank_blocks_fit_in_virtual_blocks_when_I_divides_bs(N, I, bs):
+    assert bs % I == 0
+    for L in [1, 5, bs, bs * N, bs * N + 1, 3 * bs * N - 1, 1000, 4097]:
+        sm = oracle.slot_mapping(N, I, bs, np.array([L]), np.zeros(0, np.int32), np.zeros(0, np.int64))
+        v = int(sm["virt_blocks"][0])
+        assert v == math.ceil(L / (bs * N))
+        assert np.all(sm["rank_blocks"][:, 0] <= v)
+
+
+# ------------------------------------------------------------------- slots
+
+def _random_tables(N, I, bs, seq_lens, seed):
+    sm = oracle.slot_mapping(N, I, bs, seq_lens, np.zeros(0, np.int32), np.zeros(0, np.int64))
+    tables, nblk = allocate_blocks(sm["rank_blocks"], seed=seed, spare=3)
+    return tables, nblk
+
+
+@pytest.mark.parametrize("N,I,bs", [(1, 1, 4), (2, 1, 16), (4, 4, 16), (3, 2, 8), (4, 3, 8), (8, 64, 64)])
+def test_slots_are_a_bijection(N, I, bs):
+    seq_lens = np.array([1, 7, 64, 130, 257], dtype=np.int32)
+    tables, nblk = _random_tables(N, I, bs, seq_lens, seed=N * 100 + I)
+    tok_req = np.repeat(np.arange(len(seq_lens), dtype=np.int32), seq_lens)
+    tok_pos = np.concatenate([np.arange(n) for n in seq_lens]).astype(np.int64)
+    perm = np.random.default_rng(3).permutation(tok_req.size)  # token order must not matter
+    tok_req, tok_pos = tok_req[perm], tok_pos[perm]
+    sm = oracle.slot_mapping(N, I, bs, seq_lens, tok_req, tok_pos, tables)
+    assert sm["status"] == 0
+    slots, owner = sm["slots"], sm["owner"]
+    # exactly one rank stores each token: its owner; everybody else skips (-1)
+    assert np.all((slots >= 0).sum(axis=0) == 1)
+    assert np.all(np.argmax(slots >= 0, axis=0) == owner)
+    assert np.all(owner == (tok_pos // I) % N)
+    flat = slots[slots >= 0]
+    assert flat.size == tok_req.size and np.unique(flat).size == flat.size
+    assert flat.min() >= 0 and flat.max() < nblk * bs
+    # the slot's block is in the owner's table for that request, at lpos // bs
+    for i in range(tok_req.size):
+        r, b = owner[i], tok_req[i]
+        blk, off = divmod(int(slots[r, i]), bs)
+        k = list(tables[r, b]).index(blk)
+        lp = k * bs + off
+        assert lp < sm["local_lens"][r, b]
+
+
+def test_slot_mapping_brute_force_tiny():
+    # brute force: build each rank's token list by appending tokens in order
+    for N in range(1, 5):
+        for I in range(1, 9):
+            for bs in (1, 2, 3, 8):
+                L = 37
+                lists = [[] for _ in range(N)]
+                for t in range(L):
+                    lists[(t // I) % N].append(t)
+                counts = np.array([[len(x)] for x in lists])
+                tables, _ = allocate_blocks(np.ceil(counts / bs).astype(np.int64), seed=N * 31 + I)
+                sm = oracle.slot_mapping(N, I, bs, np.array([L]), np.zeros(L, np.int32), np.arange(L), tables)
+                assert sm["status"] == 0
+                assert sm["local_lens"][:, 0].tolist() == [len(x) for x in lists]
+                for r in range(N):
+                    for idx, t in enumerate(lists[r]):
+                        assert sm["slots"][r, t] == tables[r, 0, idx // bs] * bs + idx % bs
+
+
+def test_slot_mapping_reports_bad_tokens():
+    seq_lens = np.array([10], dtype=np.int32)
+    tables, _ = _random_tables(2, 1, 4, seq_lens, seed=1)
+    sm = oracle.slot_mapping(2, 1, 4, seq_lens, np.array([0, 0, 1], np.int32), np.array([3, 10, 0]), tables)
+    assert sm["status"] == -1
+    assert sm["owner"][1] == -1 and sm["owner"][2] == -1
+    assert np.all(sm["slots"][:, 1:] == -1) and (sm["slots"][:, 0] >= 0).sum() == 1
+
+
+# ------------------------------------------------------------ storage types
+
+def test_fp8_e4m3_decode_all_codes_against_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.decode(codes, "fp8", 1.0)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan) and nan.sum() == 2
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert oracle.decode(np.array([0x7E], np.uint8), "fp8", 0.5)[0] == 224.0
+
+
+def test_bf16_decode_all_codes_against_torch():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    mine = oracle.decode(codes, "bf16")
+    ref = torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+
+
+# --------------------------------------------------------------- attention
+
+def _dense(wl):
+    c = wl.cfg
+    q = oracle.decode(wl.q, c["q_dtype"])
+    k = oracle.decode(wl.k, c["kv_dtype"], wl.kv_scale)
+    v = None if wl.v is None else oracle.decode(wl.v, c["kv_dtype"], wl.kv_scale)
+    return q, k, v
+
+
+def _sdpa_reference(wl):
+    """torch SDPA in fp64 (library routine) with an explicit causal mask."""
+    c = wl.cfg
+    B, Tq, Hq, Hkv, Dk, Dv = (int(c[x]) for x in ("B", "Tq", "Hq", "Hkv", "Dk", "Dv"))
+    q, k, v = _dense(wl)
+    outs, lses = [], []
+    for b in range(B):
+        L = int(wl.seq_lens[b])
+        s, e = int(wl.req_start[b]), int(wl.req_start[b + 1])
+        qb = torch.from_numpy(q[b]).permute(1, 0, 2)            # [Hq, Tq, Dk]
+        kb = torch.from_numpy(k[s:e]).permute(1, 0, 2)          # [Hkv, L, Dk]
+        if c["layout"] == "mla":
+            vb = kb[..., :Dv]
+        else:
+            vb = torch.from_numpy(v[s:e]).permute(1, 0, 2)
+        G = Hq // Hkv
+        kb = kb.repeat_interleave(G, dim=0)
+        vb = vb.repeat_interleave(G, dim=0)
+        pos = torch.arange(L)
+        qpos = torch.arange(L - Tq, L)
+        mask = pos[None, :] <= qpos[:, None]                    # [Tq, L]
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qb, kb, vb, attn_mask=mask, scale=float(c["softmax_scale"]))
+        scores = (qb @ kb.transpose(-1, -2)) * float(c["softmax_scale"])
+        scores = scores.masked_fill(~mask, float("-inf"))
+        lse = torch.logsumexp(scores, dim=-1)                   # [Hq, Tq]
+        outs.append(o.permute(1, 0, 2).numpy())                 # [Tq, Hq, Dv]
+        lses.append(lse.permute(1, 0).numpy())
+    return np.stack(outs).reshape(-1, Dv), np.stack(lses).reshape(-1)
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("gqa_toy", dict(L=100)),
+    ("gqa_llama8b", dict(B=2, Hq=8, Hkv=2, Dk=32, Dv=32, L=77)),
+    ("gqa_llama8b", dict(B=2, Hq=6, Hkv=3, Dk=16, Dv=24, L=40, Tq=3)),
+    ("mla_bf16_32k", dict(B=2, Hq=4, Dk=40, Dv=32, L=70)),
+    ("mla_fp8_1m", dict(Hq=4, Dk=48, Dv=32, L=90)),
+])
+def test_attention_matches_torch_sdpa(name, kw):
+    wl = make_workload(config(name, **kw), seed=5)
+    out, lse = oracle.attention(wl)
+    ref_o, ref_l = _sdpa_reference(wl)
+    assert np.abs(out - ref_o).max() < 1e-12
+    assert np.abs(lse - ref_l).max() < 1e-12
+
+
+def test_single_key_closed_form():
+    wl = make_workload(config("gqa_llama8b", B=1, Hq=4, Hkv=2, Dk=16, Dv=16, L=1), seed=2)
+    out, lse = oracle.attention(wl)
+    q, k, v = _dense(wl)
+    for h in range(4):
+        kv = h // 2
+        assert np.array_equal(out[h], v[0, kv])
+        assert lse[h] == pytest.approx(wl.cfg["softmax_scale"] * float(q[0, 0, h] @ k[0, kv]), abs=1e-13)
+
+
+def test_zero_query_gives_mean_and_log_count():
+    wl = make_workload(config("gqa_toy", L=50, Tq=3), seed=3, zero_q=True)
+    out, lse = oracle.attention(wl)
+    _, _, v = _dense(wl)
+    for t in range(3):
+        g = 50 - 3 + t + 1
+        for h in range(4):
+            row = t * 4 + h
+            assert lse[row] == pytest.approx(math.log(g), abs=1e-13)
+            assert np.abs(out[row] - v[:g, 0].mean(axis=0)).max() < 1e-13
+
+
+def test_identical_keys_give_mean():
+    wl = make_workload(config("mla_bf16_32k", B=1, Hq=3, Dk=24, Dv=16, L=33), seed=4)
+    wl.k[:] = wl.k[0]  # every token carries the same latent row
+    out, lse = oracle.attention(wl)
+    q, k, _ = _dense(wl)
+    for h in range(3):
+        s = wl.cfg["softmax_scale"] * float(q[0, 0, h] @ k[0, 0])
+        assert lse[h] == pytest.approx(s + math.log(33), abs=1e-12)
+        assert np.abs(out[h] - k[0, 0, :16]).max() < 1e-14
+
+
+# ------------------------------------------------------------------- merge
+
+@pytest.mark.parametrize("N,I", [(1, 1), (2, 1), (3, 2), (4, 1), (4, 5), (8, 1), (8, 64)])
+def test_merge_of_rank_partials_equals_unsharded(N, I):
+    cfg = config("gqa_llama8b", B=3, Hq=4, Hkv=2, Dk=16, Dv=16, Tq=2, N=N, I=I,
+                 lengths=("list", [3, 150, 600]))
+    wl = make_workload(cfg, seed=N * 10 + I)
+    full_o, full_l = oracle.attention(wl)
+    parts = [oracle.attention(wl, rank=r) for r in range(N)]
+    o_parts = np.stack([p[0] for p in parts])
+    l_parts = np.stack([p[1] for p in parts])
+    m_o, m_l = oracle.merge(o_parts, l_parts)
+    assert np.abs(m_o - full_o).max() < 1e-12
+    assert np.abs(m_l - full_l).max() < 1e-12
+    # rank order does not matter
+    perm = np.random.default_rng(N).permutation(N)
+    p_o, p_l = oracle.merge(o_parts[perm], l_parts[perm])
+    assert np.abs(p_o - m_o).max() < 1e-13 and np.abs(p_l - m_l).max() < 1e-13
+    # ranks that own none of a short request carry weight zero (-inf LSE)
+    if N * I > 3:
+        short_rows = slice(0, 2 * 4)  # request 0 (3 tokens), both query tokens
+        empty = [r for r in range(N) if oracle.local_len(3, r, N, I) == 0]
+        for r in empty:
+            assert np.all(np.isneginf(l_parts[r, short_rows]))
+            assert np.all(o_parts[r, short_rows] == 0)
+
+
+def test_merge_single_part_is_identity():
+    rng = np.random.default_rng(0)
+    o = rng.standard_normal((1, 5, 7))
+    l = rng.standard_normal((1, 5))
+    mo, ml = oracle.merge(o, l)
+    assert np.abs(mo - o[0]).max() < 1e-15 and np.abs(ml - l[0]).max() < 1e-15
+
+
+def test_merge_weights_by_lse():
+    # two parts with LSEs log(1) and log(3): weights 1/4 and 3/4, merged LSE log(4)
+    o = np.array([[[1.0, 0.0]], [[0.0, 1.0]]])
+    l = np.log(np.array([[1.0], [3.0]]))
+    mo, ml = oracle.merge(o, l)
+    assert np.allclose(mo, [[0.25, 0.75]], atol=1e-15)
+    assert ml[0] == pytest.approx(math.log(4.0), abs=1e-15)
