@@ -1,0 +1,362 @@
+"""Benchmark: one DCP decode step on one GB300 (or N independent replicas).
+
+A step is one pass of the whole hot path over one batch: slot mapping and
+cache write of the batch's new tokens into their owners' paged slots, then the
+partial attention of every virtual rank with the exact LSE merge fused in.
+
+Workload (default): MLA, 128 heads sharing one 576-wide latent (512 values),
+FP8-e4m3 cache, bf16 queries, 16 requests with mixed contexts (lognormal,
+median 67K, clipped to [4K, 200K]), N = 8 virtual ranks, interleave 1,
+block 64.  The KV bytes (~0.75 GB) exceed L2 (129 MB), so no flush is needed
+between steps.  Other workloads: --workload <name> (dcp_workloads.CONFIGS).
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle instead.
+"""
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dcp_workloads import config, make_workload  # noqa: E402
+
+METRIC = "decode-attn tokens/s and KV-read TB/s vs roofline (MLA 128h, 64K ctx, 1 GB300)"
+DEFAULT_WORKLOAD = "mla_fp8_mixed"
+ESIZE = {"f32": 4, "bf16": 2, "fp8": 1}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def algorithmic(wl):
+    """Algorithmic bytes and FLOPs of one attention launch (every KV byte read once)."""
+    c = wl.cfg
+    B, Tq, Hq, Hkv, Dk, Dv = (int(c[k]) for k in ("B", "Tq", "Hq", "Hkv", "Dk", "Dv"))
+    L = wl.seq_lens.astype(np.int64)
+    kv_row = Dk * ESIZE[c["kv_dtype"]] * Hkv + (0 if c["layout"] == "mla" else Dv * ESIZE[c["kv_dtype"]] * Hkv)
+    kv_bytes = int(L.sum()) * kv_row
+    q_bytes = B * Tq * Hq * Dk * ESIZE[c["q_dtype"]]
+    out_bytes = B * Tq * Hq * (Dv * ESIZE[c["out_dtype"]] + 4)
+    # every query row t sees L - Tq + t + 1 tokens
+    vis = sum(int(l) * Tq - Tq * (Tq - 1) // 2 for l in L)
+    flops = 2 * vis * Hq * (Dk + Dv)
+    return dict(kv_bytes=kv_bytes, bytes=kv_bytes + q_bytes + out_bytes, flops=flops)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms (best effort)."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in out.strip().splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxs.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": float(np.median(sms)), "sm_max_mhz": float(max(maxs)), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(values, world):
+    """Max over ranks of a list of floats (gloo, host tensors; no GPU collective)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_oracle_sample(wl, budget_s=20.0):
+    """Time the oracle on a bounded sample: query rows of the median-length request.
+
+    Returns (tokens_per_s scaled to the whole workload, description, threads)."""
+    import oracle
+    c = wl.cfg
+    B, Tq, Hq = int(c["B"]), int(c["Tq"]), int(c["Hq"])
+    L = wl.seq_lens.astype(np.int64)
+    b = int(np.argsort(L)[len(L) // 2])
+    threads = oracle.threads()
+    # probe with a few rows, then size the sample to ~budget_s
+    rows_all = np.array([(b * Tq + t) * Hq + h for t in range(Tq) for h in range(Hq)], dtype=np.int64)
+    n = min(len(rows_all), max(threads, 8))
+    t0 = time.perf_counter()
+    oracle.attention(wl, rows=rows_all[:n], nthreads=threads)
+    dt = time.perf_counter() - t0
+    per_row = dt / n
+    n2 = int(min(len(rows_all), max(n, budget_s / max(per_row, 1e-9))))
+    if n2 > n:
+        t0 = time.perf_counter()
+        oracle.attention(wl, rows=rows_all[:n2], nthreads=threads)
+        dt = time.perf_counter() - t0
+        n = n2
+    # seconds for the whole workload: scale by rows and by each request's context
+    rows_total = B * Tq * Hq
+    sec_workload = dt / n * rows_total * (float(L.mean()) / float(L[b]))
+    tok_s = B * Tq / sec_workload
+    desc = (f"{n} of {rows_total} query rows (request {b}, {int(L[b])} tokens), fp64 C oracle; "
+            f"scaled by rows and mean/sample context length")
+    return tok_s, desc, threads, dt
+
+
+def run_reference(args):
+    """The CPU oracle as it stands, timed on the host cores (rank 0 only)."""
+    rank, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        if rank != 0:
+            dist.barrier()
+            dist.destroy_process_group()
+            return
+    cfg = config(args.workload)
+    wl = make_workload(cfg)
+    budget = max(1.0, 120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, budget_s=budget / 4)
+    vals, times = [], []
+    for _ in range(args.steps):
+        v, desc, threads, dt = cpu_oracle_sample(wl, budget_s=budget)
+        vals.append(v)
+        times.append(dt)
+    value = float(np.median(vals))
+    c = wl.cfg
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * int(c["B"]) * int(c["Tq"]) / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; stands in for the pages' agentic ~67K-median trace)",
+        "config": workload_config(c, wl),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def workload_config(c, wl):
+    return {
+        "workload": c["name"], "layout": c["layout"], "batch": int(c["B"]), "query_tokens": int(c["Tq"]),
+        "q_heads": int(c["Hq"]), "kv_heads": int(c["Hkv"]), "key_width": int(c["Dk"]), "value_width": int(c["Dv"]),
+        "context_tokens_total": int(wl.seq_lens.sum()), "context_median": int(np.median(wl.seq_lens)),
+        "dcp_ranks": int(c["N"]), "interleave": int(c["I"]), "block_size": int(c["block_size"]),
+        "kv_dtype": c["kv_dtype"], "q_dtype": c["q_dtype"], "out_dtype": c["out_dtype"],
+        "global_batch": int(c["B"]) * int(c["Tq"]), "parallelism": "replicas (virtual DCP ranks on one GPU)",
+        "l2": "inputs larger than L2 (no flush)",
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="dcp", choices=["dcp", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import context_decode_attention_gb300 as dcp
+    from context_decode_attention_gb300.harness import DeviceWorkload, raw_to_torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = config(args.workload)
+    wl = make_workload(cfg, seed=int(cfg["index"]) + 1000 * rank)  # replicas: same shape, own data
+    dw = DeviceWorkload(wl, device=dev)
+    stream = dw.stream
+    kernel = dcp.dcp_attention_kernel(dw.params)
+    alg = algorithmic(wl)
+    peaks = load_peaks()
+
+    for _ in range(args.warmup):
+        dw.step()
+    torch.cuda.synchronize()
+    if dw.error_bits() != 0:
+        raise SystemExit("device error bits set during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = dcp.dcp_launch_count()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for k in range(K):
+            ev[k][0].record(stream)
+            dw.write_new_tokens()
+            ev[k][1].record(stream)
+            dw.decode()
+            ev[k][2].record(stream)
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = dcp.dcp_launch_count() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    write_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    if dw.error_bits() != 0:
+        raise SystemExit("device error bits set during the timed region")
+
+    # ---- end to end through the public API: host buffers in, host results out
+    e2e = None
+    if not args.no_e2e:
+        q_h = raw_to_torch(wl.q, cfg["q_dtype"]).pin_memory()
+        nk_h = dw.new_k.cpu().pin_memory()
+        nv_h = None if dw.new_v is None else dw.new_v.cpu().pin_memory()
+        req_h, pos_h = dw.new_req.cpu().pin_memory(), dw.new_pos.cpu().pin_memory()
+        sl_h = dw.seq_lens.cpu().pin_memory()
+        out_h = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+        lse_h = torch.empty(dw.lse.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in [q_h, nk_h, req_h, pos_h, sl_h] + ([nv_h] if nv_h is not None else []))
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+        for _ in range(2):
+            dw.step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(K):
+                dw.q.copy_(q_h, non_blocking=True)
+                dw.new_k.copy_(nk_h, non_blocking=True)
+                if nv_h is not None:
+                    dw.new_v.copy_(nv_h, non_blocking=True)
+                dw.new_req.copy_(req_h, non_blocking=True)
+                dw.new_pos.copy_(pos_h, non_blocking=True)
+                dw.seq_lens.copy_(sl_h, non_blocking=True)
+                dw.step()
+                out_h.copy_(dw.out, non_blocking=True)
+                lse_h.copy_(dw.lse, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max([e0.elapsed_time(e1) / K], world)[0]
+        e2e = {"value": world * int(cfg["B"]) * int(cfg["Tq"]) / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+
+    total_ms, attn_ms, write_ms = reduce_max([total_ms, attn_ms, write_ms], world)
+    ms_per_step = total_ms / K
+    tokens_per_step = int(cfg["B"]) * int(cfg["Tq"])
+    value = world * tokens_per_step / (ms_per_step / 1e3)
+
+    # roofline of the dominant kernel (attention incl. its planner launch)
+    t_attn = attn_ms / 1e3
+    t_mem = alg["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_tc > t_mem:
+        roof = {"bound": "tensor", "achieved": alg["flops"] / t_attn / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": alg["bytes"] / t_attn / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["peak_source"] = peaks["source"] + " (MEASURED_PEAKS.json, burst)"
+    roof["kernel"] = kernel
+    roof["roofline_ms"] = 1e3 * max(t_mem, t_tc)
+    roof["attn_ms"] = attn_ms
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if kernel in ("gqa_mma", "mla_tcgen05") else "f32",
+        "data": "synthetic (seeded; stands in for the pages' agentic ~67K-median trace)",
+        "config": workload_config(cfg, wl),
+        "kv_read_tbps": alg["kv_bytes"] / t_attn / 1e12,
+        "cache_write_ms": write_ms,
+        "roofline": roof,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, threads, _ = cpu_oracle_sample(wl)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

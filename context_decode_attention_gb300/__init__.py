@@ -1,0 +1,126 @@
+"""DCP decode attention on one GB300 (sm_103a): thin Python binding of libdcp.
+
+The binding only marshals arguments: every step of the path runs in the CUDA
+kernels of libdcp.so (context_decode_attention_gb300/_build/, built by
+build.py).  PyTorch supplies device memory and streams.  Nothing here falls
+back to the CPU: if the library is missing or cannot load, every call raises.
+
+Functions carry the C ABI's names (include/dcp.h):
+  dcp_workspace_size, dcp_workspace_init, dcp_get_error, dcp_slot_mapping,
+  dcp_partial_attention, dcp_lse_merge, dcp_decode_attention
+"""
+
+import ctypes
+import math
+import os
+
+from ._lib import (
+    DCP_BF16, DCP_F32, DCP_FP8_E4M3, DCP_LAYOUT_GQA, DCP_LAYOUT_MLA, DcpError, DcpParams, lib, lib_path,
+)
+
+__all__ = [
+    "DcpError", "DcpParams", "params_from_config", "lib", "lib_path",
+    "dcp_workspace_size", "dcp_workspace_init", "dcp_get_error", "dcp_slot_mapping",
+    "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention", "dcp_launch_count",
+    "dcp_attention_kernel", "DCP_F32", "DCP_BF16", "DCP_FP8_E4M3", "DCP_LAYOUT_GQA", "DCP_LAYOUT_MLA",
+]
+
+_DT = {"f32": DCP_F32, "bf16": DCP_BF16, "fp8": DCP_FP8_E4M3}
+
+
+def params_from_config(cfg, kv_scale=1.0):
+    """dcp_params for a config dict (see dcp_workloads.configs)."""
+    p = DcpParams()
+    p.N, p.I, p.block_size = int(cfg["N"]), int(cfg["I"]), int(cfg["block_size"])
+    p.layout = DCP_LAYOUT_MLA if cfg["layout"] == "mla" else DCP_LAYOUT_GQA
+    p.Hq, p.Hkv, p.Dk, p.Dv, p.Tq = (int(cfg[k]) for k in ("Hq", "Hkv", "Dk", "Dv", "Tq"))
+    p.q_dtype, p.kv_dtype, p.out_dtype = _DT[cfg["q_dtype"]], _DT[cfg["kv_dtype"]], _DT[cfg["out_dtype"]]
+    p.kv_scale = float(kv_scale)
+    p.softmax_scale = float(cfg["softmax_scale"])
+    return p
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc, what):
+    if rc != 0:
+        msg = lib().dcp_error_string(rc).decode()
+        raise DcpError(rc, f"{what}: {msg} ({rc})")
+
+
+def dcp_launch_count():
+    """Kernel launches libdcp has enqueued since load."""
+    return int(lib().dcp_launch_count())
+
+
+def dcp_attention_kernel(params):
+    """Name of the attention kernel libdcp selects for params (None if unsupported)."""
+    name = lib().dcp_attention_kernel(ctypes.byref(params))
+    return None if name is None else name.decode()
+
+
+def dcp_workspace_size(params, B, max_seq_len):
+    n = ctypes.c_size_t(0)
+    _check(lib().dcp_workspace_size(ctypes.byref(params), int(B), int(max_seq_len), ctypes.byref(n)),
+           "dcp_workspace_size")
+    return int(n.value)
+
+
+def dcp_workspace_init(workspace, stream=None):
+    _check(lib().dcp_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream)), "dcp_workspace_init")
+
+
+def dcp_get_error(workspace, stream=None):
+    bits = ctypes.c_uint32(0)
+    _check(lib().dcp_get_error(_ptr(workspace), _stream(stream), ctypes.byref(bits)), "dcp_get_error")
+    return int(bits.value)
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def dcp_slot_mapping(params, seq_lens, tok_req=None, tok_pos=None, block_tables=None, num_blocks=0,
+                     owner=None, slots=None, local_lens=None, virt_blocks=None, rank_blocks=None,
+                     new_k=None, new_v=None, k_pool=None, v_pool=None, workspace=None, stream=None):
+    B = int(seq_lens.numel())
+    T = 0 if tok_req is None else int(tok_req.numel())
+    max_blocks = 0 if block_tables is None else int(block_tables.shape[-1])
+    _check(lib().dcp_slot_mapping(ctypes.byref(params), B, _ptr(seq_lens), T, _ptr(tok_req), _ptr(tok_pos),
+                                  _ptr(block_tables), max_blocks, int(num_blocks), _ptr(owner), _ptr(slots),
+                                  _ptr(local_lens), _ptr(virt_blocks), _ptr(rank_blocks), _ptr(new_k),
+                                  _ptr(new_v), _ptr(k_pool), _ptr(v_pool), _ptr(workspace),
+                                  _nbytes(workspace), _stream(stream)), "dcp_slot_mapping")
+
+
+def dcp_partial_attention(params, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens,
+                          out_partial, lse_partial, workspace, stream=None):
+    _check(lib().dcp_partial_attention(ctypes.byref(params), int(seq_lens.numel()), _ptr(q), _ptr(k_pool),
+                                       _ptr(v_pool), int(num_blocks), _ptr(block_tables),
+                                       int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(local_lens),
+                                       _ptr(out_partial), _ptr(lse_partial), _ptr(workspace),
+                                       _nbytes(workspace), _stream(stream)), "dcp_partial_attention")
+
+
+def dcp_decode_attention(params, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens,
+                         out, lse, workspace, stream=None):
+    _check(lib().dcp_decode_attention(ctypes.byref(params), int(seq_lens.numel()), _ptr(q), _ptr(k_pool),
+                                      _ptr(v_pool), int(num_blocks), _ptr(block_tables),
+                                      int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(local_lens),
+                                      _ptr(out), _ptr(lse), _ptr(workspace), _nbytes(workspace),
+                                      _stream(stream)), "dcp_decode_attention")
+
+
+def dcp_lse_merge(N, rows, Dv, out_partial, lse_partial, out, out_dtype, lse=None, stream=None):
+    _check(lib().dcp_lse_merge(int(N), int(rows), int(Dv), _ptr(out_partial), _ptr(lse_partial), _ptr(out),
+                               int(out_dtype), _ptr(lse), _stream(stream)), "dcp_lse_merge")

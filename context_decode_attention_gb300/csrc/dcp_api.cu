@@ -1,0 +1,276 @@
+// extern "C" entry points of libdcp: host validation, kernel selection,
+// workspace layout.  See include/dcp.h for the contract of every call.
+#include <math.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "dcp_internal.cuh"
+
+namespace dcp {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+
+int device_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool valid_dtype(int d, bool allow_fp8) {
+    return d == DCP_F32 || d == DCP_BF16 || (allow_fp8 && d == DCP_FP8_E4M3);
+}
+
+int esize(int d) { return d == DCP_F32 ? 4 : (d == DCP_BF16 ? 2 : 1); }
+
+int validate_params(const dcp_params* p) {
+    if (!p) return DCP_ERR_INVALID_ARG;
+    if (p->N < 1 || p->I < 1 || p->block_size < 1) return DCP_ERR_INVALID_ARG;
+    if (p->layout != DCP_LAYOUT_GQA && p->layout != DCP_LAYOUT_MLA) return DCP_ERR_INVALID_ARG;
+    if (p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0) return DCP_ERR_INVALID_ARG;
+    if (p->Dk < 1 || p->Dv < 1 || p->Tq < 1) return DCP_ERR_INVALID_ARG;
+    if (p->layout == DCP_LAYOUT_MLA && (p->Hkv != 1 || p->Dv > p->Dk)) return DCP_ERR_INVALID_ARG;
+    if (!valid_dtype(p->q_dtype, false) || !valid_dtype(p->kv_dtype, true) || !valid_dtype(p->out_dtype, false))
+        return DCP_ERR_INVALID_ARG;
+    if (!(p->kv_scale > 0.f) || !isfinite(p->kv_scale)) return DCP_ERR_INVALID_ARG;
+    if (p->kv_dtype != DCP_FP8_E4M3 && p->kv_scale != 1.f) return DCP_ERR_INVALID_ARG;
+    if (!isfinite(p->softmax_scale)) return DCP_ERR_INVALID_ARG;
+    return DCP_OK;
+}
+
+bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15) == 0; }
+
+enum class Kernel { kNone, kGeneric, kGqaMma };
+
+const char* kernel_name(Kernel k) {
+    switch (k) {
+        case Kernel::kGqaMma: return "gqa_mma";
+        case Kernel::kGeneric: return "generic";
+        default: return nullptr;
+    }
+}
+
+Kernel select_kernel(const dcp_params& p) {
+    if (gqa_mma_supported(p)) return Kernel::kGqaMma;
+    if (generic_supported(p)) return Kernel::kGeneric;
+    return Kernel::kNone;
+}
+
+int64_t kernel_workers(Kernel k, int sms) {
+    switch (k) {
+        case Kernel::kGqaMma: return gqa_mma_workers(sms);
+        case Kernel::kGeneric: return generic_workers(sms);
+        default: return 0;
+    }
+}
+
+int kernel_chunk(Kernel k, const dcp_params& p) {
+    switch (k) {
+        case Kernel::kGqaMma: return 16;
+        case Kernel::kGeneric: return generic_chunk(p.block_size);
+        default: return 1;
+    }
+}
+
+// Workspace layout for (params, B) with the kernel that would run.
+bool layout_for(const dcp_params& p, int32_t B, WsLayout* out, Kernel* kout, int64_t* W) {
+    const int sms = device_sms();
+    if (sms <= 0) return false;
+    const Kernel k = select_kernel(p);
+    const int64_t U = (int64_t)B * p.Hkv * p.N;
+    const int64_t w = k == Kernel::kNone ? 0 : kernel_workers(k, sms);
+    const int64_t rows = (int64_t)p.Tq * (p.Hq / p.Hkv);
+    *out = ws_layout(U, U, w + U, rows, p.Dv);
+    if (kout) *kout = k;
+    if (W) *W = w;
+    return true;
+}
+
+int run_attention(const dcp_params* params, int32_t B, const void* q, const void* k_pool,
+                  const void* v_pool, int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks,
+                  const int32_t* seq_lens, const int32_t* local_lens, bool partial_mode, float* out_partial,
+                  float* lse_partial, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
+    int rc = validate_params(params);
+    if (rc != DCP_OK) return rc;
+    const dcp_params& p = *params;
+    if (B < 0) return DCP_ERR_INVALID_ARG;
+    if (B == 0) return DCP_OK;
+    if (!q || !k_pool || !block_tables || !seq_lens || !local_lens) return DCP_ERR_INVALID_ARG;
+    if (p.layout == DCP_LAYOUT_GQA && !v_pool) return DCP_ERR_INVALID_ARG;
+    if (p.layout == DCP_LAYOUT_MLA && v_pool) return DCP_ERR_INVALID_ARG;
+    if (partial_mode && (!out_partial || !lse_partial)) return DCP_ERR_INVALID_ARG;
+    if (!partial_mode && !out) return DCP_ERR_INVALID_ARG;
+    if (num_blocks < 1 || max_blocks < 1) return DCP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || (v_pool && !aligned16(v_pool))) return DCP_ERR_INVALID_ARG;
+    if (!workspace) return DCP_ERR_WORKSPACE;
+    WsLayout lay;
+    Kernel kern;
+    int64_t W;
+    if (!layout_for(p, B, &lay, &kern, &W)) return DCP_ERR_CUDA;
+    if (kern == Kernel::kNone) return DCP_ERR_UNSUPPORTED;
+    if (workspace_bytes < lay.total) return DCP_ERR_WORKSPACE;
+
+    AttnArgs a;
+    memset(&a, 0, sizeof a);
+    a.N = p.N; a.I = p.I; a.bs = p.block_size; a.Hq = p.Hq; a.Hkv = p.Hkv; a.Dk = p.Dk; a.Dv = p.Dv;
+    a.Tq = p.Tq; a.G = p.Hq / p.Hkv; a.B = B; a.max_blocks = max_blocks; a.layout = p.layout;
+    a.partial_mode = partial_mode ? 1 : 0; a.out_dtype = p.out_dtype; a.CH = kernel_chunk(kern, p);
+    a.num_blocks = num_blocks; a.U = (int64_t)B * p.Hkv * p.N;
+    a.Gn = partial_mode ? a.U : (int64_t)B * p.Hkv; a.W = W;
+    a.softmax_scale = p.softmax_scale; a.kv_scale = p.kv_scale;
+    a.q = q; a.k_pool = k_pool; a.v_pool = v_pool; a.block_tables = block_tables; a.seq_lens = seq_lens;
+    a.local_lens = local_lens; a.out_partial = out_partial; a.lse_partial = lse_partial; a.out = out;
+    a.lse = lse; a.ws = reinterpret_cast<uint8_t*>(workspace); a.lay = lay; a.rows = p.Tq * a.G;
+
+    PlanArgs pa;
+    memset(&pa, 0, sizeof pa);
+    pa.N = p.N; pa.I = p.I; pa.bs = p.block_size; pa.Hkv = p.Hkv; pa.Tq = p.Tq; pa.CH = a.CH; pa.B = B;
+    pa.partial_mode = a.partial_mode; pa.W = W; pa.max_blocks = max_blocks; pa.seq_lens = seq_lens;
+    pa.local_lens = local_lens; pa.ws = a.ws; pa.lay = lay; pa.U = a.U; pa.G = a.Gn;
+    pa.rows_per_group = a.rows; pa.Hq = p.Hq; pa.Dv = p.Dv; pa.out_partial = out_partial;
+    pa.lse_partial = lse_partial; pa.out = out; pa.lse = lse; pa.out_dtype = p.out_dtype;
+    launch_plan(pa, stream);
+    if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
+    count_launches(1);
+
+    cudaError_t e = cudaSuccess;
+    if (kern == Kernel::kGqaMma) {
+        e = launch_attn_gqa_mma(a, stream);
+        count_launches(1);
+    } else {
+        e = launch_attn_generic(a, p.q_dtype, p.kv_dtype, stream);
+        count_launches(1);
+        if (e == cudaSuccess && a.Gn > 0) {
+            e = launch_segment_merge(a, stream);
+            count_launches(1);
+        }
+    }
+    return e == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace dcp
+
+using namespace dcp;
+
+extern "C" {
+
+int dcp_version(void) { return 1; }
+
+uint64_t dcp_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* dcp_attention_kernel(const dcp_params* params) {
+    if (validate_params(params) != DCP_OK) return nullptr;
+    return kernel_name(select_kernel(*params));
+}
+
+const char* dcp_error_string(int code) {
+    switch (code) {
+        case DCP_OK: return "ok";
+        case DCP_ERR_INVALID_ARG: return "invalid argument";
+        case DCP_ERR_UNSUPPORTED: return "unsupported combination";
+        case DCP_ERR_CUDA: return "CUDA runtime error";
+        case DCP_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown error code";
+    }
+}
+
+int dcp_workspace_size(const dcp_params* params, int32_t B, int64_t max_seq_len, size_t* bytes) {
+    int rc = validate_params(params);
+    if (rc != DCP_OK) return rc;
+    if (!bytes || B < 0 || max_seq_len < 1) return DCP_ERR_INVALID_ARG;
+    WsLayout lay;
+    Kernel k;
+    if (!layout_for(*params, B, &lay, &k, nullptr)) return DCP_ERR_CUDA;
+    *bytes = lay.total;
+    return DCP_OK;
+}
+
+int dcp_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!workspace || workspace_bytes < 256) return DCP_ERR_WORKSPACE;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, stream) == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
+int dcp_get_error(void* workspace, cudaStream_t stream, uint32_t* bits) {
+    if (!workspace || !bits) return DCP_ERR_INVALID_ARG;
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return DCP_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return DCP_ERR_CUDA;
+    *bits = v;
+    if (v != 0) {
+        if (cudaMemsetAsync(workspace, 0, sizeof v, stream) != cudaSuccess) return DCP_ERR_CUDA;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return DCP_ERR_CUDA;
+    }
+    return DCP_OK;
+}
+
+int dcp_slot_mapping(const dcp_params* params, int32_t B, const int32_t* seq_lens, int64_t T,
+                     const int32_t* tok_req, const int64_t* tok_pos, const int32_t* block_tables,
+                     int32_t max_blocks, int64_t num_blocks, int8_t* owner, int64_t* slots,
+                     int32_t* local_lens, int32_t* virt_blocks, int32_t* rank_blocks, const void* new_k,
+                     const void* new_v, void* k_pool, void* v_pool, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
+    int rc = validate_params(params);
+    if (rc != DCP_OK) return rc;
+    const dcp_params& p = *params;
+    if (B < 0 || T < 0) return DCP_ERR_INVALID_ARG;
+    if (B > 0 && !seq_lens) return DCP_ERR_INVALID_ARG;
+    if (T > 0 && (owner || slots || new_k) && (!tok_req || !tok_pos)) return DCP_ERR_INVALID_ARG;
+    if (T > 0 && B == 0 && (owner || slots || new_k)) return DCP_ERR_INVALID_ARG;
+    if ((slots || new_k) && (!block_tables || max_blocks < 1 || num_blocks < 1)) return DCP_ERR_INVALID_ARG;
+    if (new_k && !k_pool) return DCP_ERR_INVALID_ARG;
+    if (p.layout == DCP_LAYOUT_GQA && new_k && (!new_v || !v_pool)) return DCP_ERR_INVALID_ARG;
+    if (p.layout == DCP_LAYOUT_MLA && (new_v || v_pool)) return DCP_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < 256) return DCP_ERR_WORKSPACE;
+    SlotArgs a;
+    memset(&a, 0, sizeof a);
+    a.N = p.N; a.I = p.I; a.bs = p.block_size; a.B = B; a.layout = p.layout; a.Hkv = p.Hkv; a.Dk = p.Dk;
+    a.Dv = p.Dv; a.kv_esize = esize(p.kv_dtype); a.max_blocks = max_blocks; a.T = T; a.num_blocks = num_blocks;
+    a.seq_lens = seq_lens; a.tok_req = tok_req; a.tok_pos = tok_pos; a.block_tables = block_tables;
+    a.owner = owner; a.slots = slots; a.local_lens = local_lens; a.virt_blocks = virt_blocks;
+    a.rank_blocks = rank_blocks; a.new_k = new_k; a.new_v = new_v; a.k_pool = k_pool; a.v_pool = v_pool;
+    a.err = &reinterpret_cast<WsHeader*>(workspace)->err;
+    return launch_slot_mapping(a, stream) == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
+int dcp_partial_attention(const dcp_params* params, int32_t B, const void* q, const void* k_pool,
+                          const void* v_pool, int64_t num_blocks, const int32_t* block_tables,
+                          int32_t max_blocks, const int32_t* seq_lens, const int32_t* local_lens,
+                          float* out_partial, float* lse_partial, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
+    return run_attention(params, B, q, k_pool, v_pool, num_blocks, block_tables, max_blocks, seq_lens,
+                         local_lens, true, out_partial, lse_partial, nullptr, nullptr, workspace,
+                         workspace_bytes, stream);
+}
+
+int dcp_decode_attention(const dcp_params* params, int32_t B, const void* q, const void* k_pool,
+                         const void* v_pool, int64_t num_blocks, const int32_t* block_tables,
+                         int32_t max_blocks, const int32_t* seq_lens, const int32_t* local_lens, void* out,
+                         float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return run_attention(params, B, q, k_pool, v_pool, num_blocks, block_tables, max_blocks, seq_lens,
+                         local_lens, false, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream);
+}
+
+int dcp_lse_merge(int32_t N, int64_t rows, int32_t Dv, const float* out_partial, const float* lse_partial,
+                  void* out, int32_t out_dtype, float* lse, cudaStream_t stream) {
+    if (N < 1 || rows < 0 || Dv < 1) return DCP_ERR_INVALID_ARG;
+    if (out_dtype != DCP_F32 && out_dtype != DCP_BF16) return DCP_ERR_INVALID_ARG;
+    if (rows == 0) return DCP_OK;
+    if (!out_partial || !lse_partial || !out) return DCP_ERR_INVALID_ARG;
+    return launch_lse_merge(N, rows, Dv, out_partial, lse_partial, out, out_dtype, lse, stream) == cudaSuccess
+               ? DCP_OK
+               : DCP_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,203 @@
+// Internal declarations shared by the libdcp translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/dcp.h"
+
+namespace dcp {
+
+// ---------------------------------------------------------------------------
+// Interleaved ownership, closed forms.
+// ("Breaking the Long-Sequence Inference Bottleneck ...", section 2: rank of
+// token t is floor(t / I) mod N; "vLLM DCP and PCP", Deep Dive 5: the local
+// lengths.)  A rank stores its tokens in token order, so token t sits at local
+// position floor(t / (N I)) * I + t mod I, and the first L tokens leave
+// floor(L / (N I)) * I + clamp(L mod (N I) - r I, 0, I) tokens on rank r.
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int64_t owner_rank(int64_t t, int N, int I) {
+    return (t / I) % N;
+}
+__host__ __device__ __forceinline__ int64_t local_pos(int64_t t, int N, int I) {
+    const int64_t period = (int64_t)N * I;
+    return (t / period) * I + t % I;
+}
+__host__ __device__ __forceinline__ int64_t local_len(int64_t L, int r, int N, int I) {
+    const int64_t period = (int64_t)N * I;
+    int64_t extra = L % period - (int64_t)r * I;
+    extra = extra < 0 ? 0 : (extra > I ? I : extra);
+    return (L / period) * I + extra;
+}
+__host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------
+// Workspace layout (all offsets 256-byte aligned):
+//   header        256 B: error word, total chunk count
+//   unit_start    int64[U + 1]   chunk prefix over units u = (b*Hkv + kvh)*N + r
+//   seg_base      int32[G + 1]   partial-slot prefix over merge groups
+//   counters      uint32[G]      arrivals per group (fused merge)
+//   part_o        fp32[seg_max][rows][Dv]
+//   part_lse      fp32[seg_max][rows]
+// ---------------------------------------------------------------------------
+struct WsHeader {
+    uint32_t err;
+    uint32_t pad;
+    int64_t total_chunks;
+};
+
+struct WsLayout {
+    size_t off_units, off_seg_base, off_counters, off_part_o, off_part_lse, total;
+};
+
+__host__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+__host__ inline WsLayout ws_layout(int64_t U, int64_t G, int64_t seg_max, int64_t rows, int64_t Dv) {
+    WsLayout l;
+    size_t o = 256;
+    l.off_units = o; o = align256(o + sizeof(int64_t) * (size_t)(U + 1));
+    l.off_seg_base = o; o = align256(o + sizeof(int32_t) * (size_t)(G + 1));
+    l.off_counters = o; o = align256(o + sizeof(uint32_t) * (size_t)(G + 1));
+    l.off_part_o = o; o = align256(o + sizeof(float) * (size_t)seg_max * rows * Dv);
+    l.off_part_lse = o; o = align256(o + sizeof(float) * (size_t)seg_max * rows);
+    l.total = o;
+    return l;
+}
+
+// Count kernel launches (dcp_launch_count).
+void count_launches(int n);
+
+// Raise device error bits.
+__device__ __forceinline__ void raise_err(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
+
+// Which worker (of W over P chunks, worker w owning [w*P/W, (w+1)*P/W)) owns chunk x.
+__host__ __device__ __forceinline__ int64_t worker_of(int64_t x, int64_t W, int64_t P) {
+    return ((x + 1) * W - 1) / P;
+}
+__host__ __device__ __forceinline__ int64_t worker_begin(int64_t w, int64_t W, int64_t P) {
+    return w * P / W;
+}
+
+// ---------------------------------------------------------------------------
+// The work plan shared by the attention kernels.
+//   unit u = ((b * Hkv + kvh) * N + r): rank r's tokens of request b, KV head kvh;
+//   chunk: CH consecutive local positions of one unit (CH divides block_size
+//   or is a multiple of it that stays inside one block);
+//   merge group: decode mode = (b, kvh) (all ranks), partial mode = unit.
+// ---------------------------------------------------------------------------
+struct PlanArgs {
+    int N, I, bs, Hkv, Tq, CH;
+    int B;
+    int partial_mode;  // 0: groups (b, kvh); 1: groups (b, kvh, r)
+    int64_t W;         // workers of the attention kernel that follows
+    int max_blocks;
+    const int32_t* seq_lens;
+    const int32_t* local_lens;
+    uint8_t* ws;
+    WsLayout lay;
+    int64_t U, G;
+    // outputs for groups that own no chunk
+    int rows_per_group;   // Tq * (Hq / Hkv)
+    int Hq, Dv;
+    float* out_partial;   // partial mode
+    float* lse_partial;
+    void* out;            // decode mode
+    float* lse;
+    int out_dtype;
+};
+
+void launch_plan(const PlanArgs& a, cudaStream_t s);
+
+// Attention arguments common to the kernels.
+struct AttnArgs {
+    int N, I, bs, Hq, Hkv, Dk, Dv, Tq, G;  // G = Hq / Hkv (query heads per KV head)
+    int B, max_blocks, layout, partial_mode, out_dtype, CH;
+    int64_t num_blocks, U, Gn, W;           // Gn: merge groups
+    float softmax_scale, kv_scale;
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const int32_t* local_lens;
+    float* out_partial;
+    float* lse_partial;
+    void* out;
+    float* lse;
+    uint8_t* ws;
+    WsLayout lay;
+    int rows;  // rows per group = Tq * G
+};
+
+// generic CUDA-core path (any dtype / width); writes all segment partials,
+// then launch_segment_merge combines them.
+bool generic_supported(const dcp_params& p);
+int64_t generic_workers(int num_sms);
+int generic_chunk(int bs);
+cudaError_t launch_attn_generic(const AttnArgs& a, int q_dtype, int kv_dtype, cudaStream_t s);
+cudaError_t launch_segment_merge(const AttnArgs& a, cudaStream_t s);
+
+// bf16 GQA path on mma.sync with query-group packing and a fused merge.
+bool gqa_mma_supported(const dcp_params& p);
+int64_t gqa_mma_workers(int num_sms);
+cudaError_t launch_attn_gqa_mma(const AttnArgs& a, cudaStream_t s);
+
+// standalone merge for dcp_lse_merge
+cudaError_t launch_lse_merge(int N, int64_t rows, int Dv, const float* o_parts, const float* lse_parts,
+                             void* out, int out_dtype, float* lse, cudaStream_t s);
+
+// slot mapping + cache write
+struct SlotArgs {
+    int N, I, bs, B, layout, Hkv, Dk, Dv, kv_esize, max_blocks;
+    int64_t T, num_blocks;
+    const int32_t* seq_lens;
+    const int32_t* tok_req;
+    const int64_t* tok_pos;
+    const int32_t* block_tables;
+    int8_t* owner;
+    int64_t* slots;
+    int32_t* local_lens;
+    int32_t* virt_blocks;
+    int32_t* rank_blocks;
+    const void* new_k;
+    const void* new_v;
+    void* k_pool;
+    void* v_pool;
+    uint32_t* err;
+};
+cudaError_t launch_slot_mapping(const SlotArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Small device helpers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float(((uint32_t)b) << 16);
+}
+
+// fp8 e4m3fn -> fp32 through the hardware pair conversion (e4m3x2 -> f16x2).
+__device__ __forceinline__ float2 fp8x2_to_float2(uint16_t two) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+    __half2 h = *reinterpret_cast<__half2*>(&h2);
+    return __half22float2(h);
+}
+
+__device__ __forceinline__ float load_elem(const void* base, int64_t idx, int dtype) {
+    if (dtype == DCP_F32) return reinterpret_cast<const float*>(base)[idx];
+    if (dtype == DCP_BF16) return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(base)[idx]);
+    // fp8: decode one byte (pair conversion with a zero partner)
+    const uint8_t v = reinterpret_cast<const uint8_t*>(base)[idx];
+    return fp8x2_to_float2((uint16_t)v).x;
+}
+
+__device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int dtype) {
+    if (dtype == DCP_F32)
+        reinterpret_cast<float*>(out)[idx] = v;
+    else
+        reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+}
+
+}  // namespace dcp

@@ -1,0 +1,153 @@
+// Work plan for the split-KV attention kernels.
+//
+// Every virtual rank's local KV of every (request, KV head) is a "unit"; a
+// unit is cut into chunks of CH local tokens; the chunks of all units, in
+// unit order, are dealt to W workers as equal contiguous ranges (worker w
+// owns chunks [w P / W, (w + 1) P / W)).  A worker's range can cross unit
+// boundaries; each piece it owns of one merge group is a "segment" with its
+// own partial (o, lse) slot.  The plan is computed on the device so the host
+// never needs the lengths.
+#include "dcp_internal.cuh"
+
+namespace dcp {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+// Inclusive block-wide scan of one int64 per thread.
+__device__ int64_t block_inclusive_scan(int64_t v, int64_t* warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t t = (lane < (int)(blockDim.x >> 5)) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t n = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += n;
+        }
+        warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const int64_t before = warp > 0 ? warp_tot[warp - 1] : 0;
+    __syncthreads();
+    return v + before;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
+    __shared__ int64_t warp_tot[32];
+    __shared__ int64_t carry;
+    __shared__ int empty_flag[kPlanThreads];
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
+    int64_t* unit_start = reinterpret_cast<int64_t*>(a.ws + a.lay.off_units);
+    int32_t* seg_base = reinterpret_cast<int32_t*>(a.ws + a.lay.off_seg_base);
+    uint32_t* counters = reinterpret_cast<uint32_t*>(a.ws + a.lay.off_counters);
+    const int tid = threadIdx.x;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+
+    // 1. chunks per unit, with the metadata checks
+    for (int64_t base = 0; base < a.U; base += kPlanThreads) {
+        const int64_t u = base + tid;
+        int64_t c = 0;
+        if (u < a.U) {
+            const int r = (int)(u % a.N);
+            const int64_t bk = u / a.N;
+            const int b = (int)(bk / a.Hkv);
+            const int64_t L = a.seq_lens[b];
+            if (L < a.Tq) {
+                raise_err(&hdr->err, DCP_DEV_ERR_TOKEN);
+            } else {
+                int64_t n = a.local_lens[(int64_t)r * a.B + b];
+                const int64_t expect = local_len(L, r, a.N, a.I);
+                if (n != expect) raise_err(&hdr->err, DCP_DEV_ERR_STALE);
+                n = n < expect ? n : expect;
+                if (n < 0) n = 0;
+                if (ceil_div64(n, a.bs) > a.max_blocks) {
+                    raise_err(&hdr->err, DCP_DEV_ERR_TABLE);
+                    n = (int64_t)a.max_blocks * a.bs;
+                }
+                c = ceil_div64(n, a.CH);
+            }
+        }
+        const int64_t incl = block_inclusive_scan(c, warp_tot);
+        if (u < a.U) unit_start[u] = carry + incl - c;
+        __syncthreads();
+        if (tid == kPlanThreads - 1) carry += incl;
+        __syncthreads();
+    }
+    const int64_t P = carry;
+    if (tid == 0) {
+        unit_start[a.U] = P;
+        hdr->total_chunks = P;
+    }
+    __syncthreads();
+    if (tid == 0) carry = 0;
+    __syncthreads();
+
+    // 2. segments per merge group
+    const int64_t per_group = a.partial_mode ? 1 : a.N;
+    for (int64_t base = 0; base < a.G; base += kPlanThreads) {
+        const int64_t g = base + tid;
+        int64_t cnt = 0;
+        if (g < a.G) {
+            const int64_t first = unit_start[g * per_group];
+            const int64_t end = unit_start[(g + 1) * per_group];
+            if (end > first) cnt = worker_of(end - 1, a.W, P) - worker_of(first, a.W, P) + 1;
+            counters[g] = 0;
+        }
+        const int64_t incl = block_inclusive_scan(cnt, warp_tot);
+        if (g < a.G) seg_base[g] = (int32_t)(carry + incl - cnt);
+        __syncthreads();
+        if (tid == kPlanThreads - 1) carry += incl;
+        __syncthreads();
+    }
+    if (tid == 0) seg_base[a.G] = (int32_t)carry;
+
+    // 3. groups that own no chunk: zeros and -inf
+    const int G = a.Hq / a.Hkv;
+    for (int64_t base = 0; base < a.G; base += kPlanThreads) {
+        const int64_t g = base + tid;
+        empty_flag[tid] = (g < a.G) && unit_start[g * per_group] == unit_start[(g + 1) * per_group];
+        __syncthreads();
+        for (int k = 0; k < kPlanThreads && base + k < a.G; ++k) {
+            if (!empty_flag[k]) continue;
+            const int64_t gg = base + k;
+            int b, kvh, r = 0;
+            if (a.partial_mode) {
+                r = (int)(gg % a.N);
+                b = (int)((gg / a.N) / a.Hkv);
+                kvh = (int)((gg / a.N) % a.Hkv);
+            } else {
+                b = (int)(gg / a.Hkv);
+                kvh = (int)(gg % a.Hkv);
+            }
+            const int64_t total = (int64_t)a.rows_per_group * a.Dv;
+            for (int64_t e = tid; e < total; e += kPlanThreads) {
+                const int row = (int)(e / a.Dv), d = (int)(e % a.Dv);
+                const int t = row / G, gq = row % G;
+                const int64_t orow = ((int64_t)b * a.Tq + t) * a.Hq + (int64_t)kvh * G + gq;
+                if (a.partial_mode) {
+                    const int64_t prow = (int64_t)r * a.B * a.Tq * a.Hq + orow;
+                    a.out_partial[prow * a.Dv + d] = 0.f;
+                    if (d == 0) a.lse_partial[prow] = -INFINITY;
+                } else {
+                    store_out(a.out, orow * a.Dv + d, 0.f, a.out_dtype);
+                    if (d == 0 && a.lse) a.lse[orow] = -INFINITY;
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+void launch_plan(const PlanArgs& a, cudaStream_t s) { plan_kernel<<<1, kPlanThreads, 0, s>>>(a); }
+
+}  // namespace dcp

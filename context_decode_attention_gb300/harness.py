@@ -1,0 +1,152 @@
+"""Device-side setup of a synthetic workload for the tests, smoke() and the bench.
+
+Takes a dcp_workloads.Workload (host arrays) and builds what a serving engine
+would hold on the GPU: the query batch, per-rank block tables over one
+physical pool, and the paged cache, filled through libdcp's own slot mapping
+and cache write.  torch only allocates and copies; every computation is a
+libdcp call.
+"""
+
+import numpy as np
+import torch
+
+from dcp_workloads import allocate_blocks
+
+from . import (
+    dcp_decode_attention, dcp_get_error, dcp_lse_merge, dcp_partial_attention, dcp_slot_mapping,
+    dcp_workspace_init, dcp_workspace_size, params_from_config,
+)
+
+_TORCH_STORAGE = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8}
+
+
+def raw_to_torch(arr, dtype):
+    """Host raw storage (float32 / uint16 bf16 bits / uint8 fp8 bits) as a torch tensor."""
+    arr = np.ascontiguousarray(arr)
+    if dtype == "bf16":
+        return torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(arr)
+
+
+class DeviceWorkload:
+    """A workload resident in HBM: q, paged KV pool, block tables, metadata."""
+
+    def __init__(self, wl, device="cuda:0", populate=True, spare_blocks=0, stream=None):
+        self.wl = wl
+        self.cfg = c = wl.cfg
+        self.dev = torch.device(device)
+        self.stream = stream or torch.cuda.current_stream(self.dev)
+        self.params = params_from_config(c, wl.kv_scale)
+        self.B, self.Tq, self.Hq = int(c["B"]), int(c["Tq"]), int(c["Hq"])
+        self.Hkv, self.Dk, self.Dv = int(c["Hkv"]), int(c["Dk"]), int(c["Dv"])
+        self.N, self.bs = int(c["N"]), int(c["block_size"])
+        self.mla = c["layout"] == "mla"
+        dev = self.dev
+        self.seq_lens = torch.from_numpy(wl.seq_lens.astype(np.int32)).to(dev)
+        self.ws_bytes = dcp_workspace_size(self.params, self.B, int(wl.seq_lens.max()))
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        dcp_workspace_init(self.workspace, self.stream)
+
+        # 1. per-rank lengths and block needs (libdcp metadata)
+        self.local_lens = torch.empty((self.N, self.B), dtype=torch.int32, device=dev)
+        self.virt_blocks = torch.empty(self.B, dtype=torch.int32, device=dev)
+        self.rank_blocks = torch.empty((self.N, self.B), dtype=torch.int32, device=dev)
+        dcp_slot_mapping(self.params, self.seq_lens, local_lens=self.local_lens, virt_blocks=self.virt_blocks,
+                         rank_blocks=self.rank_blocks, workspace=self.workspace, stream=self.stream)
+        self.stream.synchronize()
+        # 2. physical blocks: a seeded random permutation of the pool
+        tables, self.num_blocks = allocate_blocks(self.rank_blocks.cpu().numpy(), seed=wl.seed,
+                                                  spare=spare_blocks)
+        self.block_tables_host = tables
+        self.block_tables = torch.from_numpy(tables).to(dev)
+        # 3. the pool and the query batch
+        kvt = _TORCH_STORAGE[c["kv_dtype"]]
+        if self.mla:
+            self.k_pool = torch.zeros((self.num_blocks, self.bs, self.Dk), dtype=kvt, device=dev)
+            self.v_pool = None
+        else:
+            self.k_pool = torch.zeros((self.num_blocks, self.Hkv, self.bs, self.Dk), dtype=kvt, device=dev)
+            self.v_pool = torch.zeros((self.num_blocks, self.Hkv, self.bs, self.Dv), dtype=kvt, device=dev)
+        self.q = raw_to_torch(wl.q, c["q_dtype"]).to(dev)
+        ot = torch.float32 if c["out_dtype"] == "f32" else torch.bfloat16
+        self.out = torch.empty((self.B, self.Tq, self.Hq, self.Dv), dtype=ot, device=dev)
+        self.lse = torch.empty((self.B, self.Tq, self.Hq), dtype=torch.float32, device=dev)
+        self.out_partial = None
+        self.lse_partial = None
+        # the newest Tq tokens of every request: the decode step's cache writes
+        nr, npos = wl.new_token_lists()
+        self.new_req = torch.from_numpy(nr).to(dev)
+        self.new_pos = torch.from_numpy(npos).to(dev)
+        rows = (wl.req_start[:-1][nr] + npos).astype(np.int64)
+        self.new_k = raw_to_torch(wl.k[rows], c["kv_dtype"]).to(dev)
+        self.new_v = None if wl.v is None else raw_to_torch(wl.v[rows], c["kv_dtype"]).to(dev)
+        if populate:
+            self.populate()
+
+    # -- cache fill -------------------------------------------------------------
+    def populate(self, chunk_tokens=1 << 20):
+        """Write every token of every request into its owner's slot (libdcp scatter)."""
+        wl, c = self.wl, self.cfg
+        tok_req, tok_pos = wl.token_lists()
+        T = tok_req.size
+        for s in range(0, T, chunk_tokens):
+            e = min(T, s + chunk_tokens)
+            req = torch.from_numpy(tok_req[s:e]).to(self.dev)
+            pos = torch.from_numpy(tok_pos[s:e]).to(self.dev)
+            nk = raw_to_torch(wl.k[s:e], c["kv_dtype"]).to(self.dev)
+            nv = None if wl.v is None else raw_to_torch(wl.v[s:e], c["kv_dtype"]).to(self.dev)
+            dcp_slot_mapping(self.params, self.seq_lens, req, pos, self.block_tables, self.num_blocks,
+                             new_k=nk, new_v=nv, k_pool=self.k_pool, v_pool=self.v_pool,
+                             workspace=self.workspace, stream=self.stream)
+        self.stream.synchronize()
+
+    # -- the hot path -------------------------------------------------------------
+    def write_new_tokens(self):
+        """Slot mapping + cache write of the step's Tq new tokens per request."""
+        dcp_slot_mapping(self.params, self.seq_lens, self.new_req, self.new_pos, self.block_tables,
+                         self.num_blocks, new_k=self.new_k, new_v=self.new_v, k_pool=self.k_pool,
+                         v_pool=self.v_pool, workspace=self.workspace, stream=self.stream)
+
+    def decode(self):
+        dcp_decode_attention(self.params, self.q, self.k_pool, self.v_pool, self.num_blocks, self.block_tables,
+                             self.seq_lens, self.local_lens, self.out, self.lse, self.workspace, self.stream)
+        return self.out, self.lse
+
+    def step(self):
+        """One decode step: cache write of the new tokens, then fused attention + merge."""
+        self.write_new_tokens()
+        return self.decode()
+
+    def partial(self):
+        if self.out_partial is None:
+            self.out_partial = torch.empty((self.N, self.B, self.Tq, self.Hq, self.Dv), dtype=torch.float32,
+                                           device=self.dev)
+            self.lse_partial = torch.empty((self.N, self.B, self.Tq, self.Hq), dtype=torch.float32,
+                                           device=self.dev)
+        dcp_partial_attention(self.params, self.q, self.k_pool, self.v_pool, self.num_blocks, self.block_tables,
+                              self.seq_lens, self.local_lens, self.out_partial, self.lse_partial,
+                              self.workspace, self.stream)
+        return self.out_partial, self.lse_partial
+
+    def merge(self, out=None, lse=None):
+        """dcp_lse_merge of the current partials into out/lse."""
+        rows = self.B * self.Tq * self.Hq
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
+        dcp_lse_merge(self.N, rows, self.Dv, self.out_partial, self.lse_partial, out, self.params.out_dtype, lse,
+                      self.stream)
+        return out, lse
+
+    def slot_mapping(self, tok_req, tok_pos):
+        """owner / slots for given tokens (host arrays in, device tensors out)."""
+        T = len(tok_req)
+        req = torch.from_numpy(np.ascontiguousarray(tok_req, dtype=np.int32)).to(self.dev)
+        pos = torch.from_numpy(np.ascontiguousarray(tok_pos, dtype=np.int64)).to(self.dev)
+        owner = torch.empty(T, dtype=torch.int8, device=self.dev)
+        slots = torch.empty((self.N, T), dtype=torch.int64, device=self.dev)
+        dcp_slot_mapping(self.params, self.seq_lens, req, pos, self.block_tables, self.num_blocks, owner=owner,
+                         slots=slots, workspace=self.workspace, stream=self.stream)
+        return owner, slots
+
+    def error_bits(self):
+        return dcp_get_error(self.workspace, self.stream)

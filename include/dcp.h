@@ -1,0 +1,215 @@
+/*
+ * dcp.h -- C ABI of libdcp: decode-context-parallel (DCP) decode attention on
+ * one GPU (sm_103a).
+ *
+ * The method (sources are the pages' titles and sections):
+ *  - "Breaking the Long-Sequence Inference Bottleneck: A Deep Dive into vLLM's
+ *    Distributed Context Parallelism Architecture", section 2 (interleaved
+ *    storage and virtual blocks): token t of a request belongs to rank
+ *    floor(t / I) mod N; a virtual block is block_size x N tokens; tokens a
+ *    rank does not own get slot -1 and are skipped by the cache write.
+ *  - "vLLM DCP and PCP: Decode and Prefill Context Parallelism", Deep Dive 5
+ *    (per-rank local lengths: every rank's attention sees its local KV prefix)
+ *    and Deep Dive 6 (each rank computes a partial output o_i and its
+ *    log-sum-exp L_i over its own KV shard; the exact global output is
+ *    O = sum_i a_i o_i / sum_i a_i with a_i = exp(L_i - max_j L_j) and
+ *    L = max_j L_j + log sum_i a_i).
+ *  - "vLLM Decode Context Parallelism for Long Context Workloads", "The DCP
+ *    Execution Process" (every rank uses the full query against its local KV
+ *    slice, then partial results are merged with their LSE values).
+ *
+ * Here all N ranks are virtual: their KV shards live in one physical block
+ * pool on one GPU, and the merge runs through device memory, not collectives.
+ *
+ * Conventions for every call:
+ *  - All pointers except `params`, `bytes` and `bits` are DEVICE pointers,
+ *    owned and allocated by the caller.  The library allocates nothing; the
+ *    only scratch is the caller's workspace (see dcp_workspace_size).
+ *  - Work is enqueued on `stream` (asynchronous); nothing synchronizes except
+ *    dcp_get_error.
+ *  - Integers: seq/local lengths int32, token positions and slots int64.
+ *  - Host-side validation returns DCP_ERR_INVALID_ARG / DCP_ERR_UNSUPPORTED
+ *    before anything is enqueued.  Device-side checks never trap: a bad block
+ *    id, token or stale length sets a bit in the workspace's error word and
+ *    the offending access is skipped; read it with dcp_get_error.
+ *
+ * Data layouts (row-major, innermost last):
+ *  - q           [B][Tq][Hq][Dk]          q_dtype (f32 or bf16)
+ *  - GQA pools   k_pool [num_blocks][Hkv][block_size][Dk],
+ *                v_pool [num_blocks][Hkv][block_size][Dv]      kv_dtype
+ *  - MLA pool    k_pool [num_blocks][block_size][Dk] (latent + RoPE row);
+ *                v_pool = NULL: values are the first Dv columns of that row
+ *  - a slot s addresses block s / block_size, offset s % block_size
+ *  - block_tables [N][B][max_blocks] int32: block ids of rank r's local
+ *                blocks for request b, in local order (unused entries: any)
+ *  - seq_lens    [B] global length of each request, including its Tq newest
+ *                tokens (the queries); query t sees global positions
+ *                0 .. seq_lens[b] - Tq + t
+ *  - local_lens  [N][B] tokens of request b that rank r owns
+ *  - out         [B][Tq][Hq][Dv] out_dtype;  lse [B][Tq][Hq] fp32 (natural log)
+ *  - out_partial [N][B][Tq][Hq][Dv] fp32;  lse_partial [N][B][Tq][Hq] fp32;
+ *                a rank with no visible token gives zeros and -inf.
+ *  - GQA head mapping: query head h reads KV head h / (Hq / Hkv).
+ */
+#ifndef DCP_H_
+#define DCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+#define DCP_OK 0
+#define DCP_ERR_INVALID_ARG 1   /* a shape, pointer or enum failed host validation */
+#define DCP_ERR_UNSUPPORTED 2   /* valid, but no kernel here handles this combination */
+#define DCP_ERR_CUDA 3          /* a CUDA runtime call failed (launch, copy, attribute) */
+#define DCP_ERR_WORKSPACE 4     /* workspace NULL or smaller than dcp_workspace_size */
+
+/* bits of the device error word (dcp_get_error) */
+#define DCP_DEV_ERR_BLOCK_ID 0x1u   /* a block id outside [0, num_blocks) was read */
+#define DCP_DEV_ERR_TOKEN 0x2u      /* a token's request or position lies outside its request */
+#define DCP_DEV_ERR_TABLE 0x4u      /* a rank needs more blocks than max_blocks */
+#define DCP_DEV_ERR_STALE 0x8u      /* local_lens disagree with seq_lens under (N, I) */
+#define DCP_DEV_ERR_TIMEOUT 0x10u   /* a bounded wait inside a kernel gave up */
+
+typedef enum { DCP_F32 = 0, DCP_BF16 = 1, DCP_FP8_E4M3 = 2 } dcp_dtype;
+typedef enum { DCP_LAYOUT_GQA = 0, DCP_LAYOUT_MLA = 1 } dcp_layout;
+
+typedef struct dcp_params {
+    int32_t N;             /* virtual DCP ranks, >= 1 */
+    int32_t I;             /* interleave size: consecutive tokens per rank turn, >= 1 */
+    int32_t block_size;    /* tokens per physical block of one rank, >= 1 */
+    int32_t layout;        /* dcp_layout */
+    int32_t Hq;            /* query heads */
+    int32_t Hkv;           /* KV heads (MLA: 1, shared by every query head) */
+    int32_t Dk;            /* key width (MLA: latent + RoPE, e.g. 512 + 64) */
+    int32_t Dv;            /* value width (MLA: <= Dk, the leading columns) */
+    int32_t Tq;            /* query tokens per request, >= 1 (1 = plain decode) */
+    int32_t q_dtype;       /* DCP_F32 or DCP_BF16 */
+    int32_t kv_dtype;      /* DCP_F32, DCP_BF16 or DCP_FP8_E4M3 */
+    int32_t out_dtype;     /* DCP_F32 or DCP_BF16 */
+    float kv_scale;        /* fp8 KV: stored value x kv_scale; otherwise must be 1 */
+    float softmax_scale;   /* scores are softmax_scale * (q . k) */
+} dcp_params;
+
+/* Library ABI version (this header: 1). */
+int dcp_version(void);
+
+/* Static text for a return code. */
+const char* dcp_error_string(int code);
+
+/* Kernel launches this library has enqueued since it was loaded (all
+ * devices, all calls): lets a caller count the GPU work of a region. */
+uint64_t dcp_launch_count(void);
+
+/* Name of the attention kernel that dcp_partial_attention and
+ * dcp_decode_attention select for these params ("gqa_mma", "mla_tcgen05",
+ * "generic"), or NULL if the params are invalid or no kernel supports them. */
+const char* dcp_attention_kernel(const dcp_params* params);
+
+/*
+ * Bytes of scratch that dcp_partial_attention / dcp_decode_attention /
+ * dcp_slot_mapping need for these params and batch size B on the CURRENT
+ * device (the bound depends on its SM count).  max_seq_len bounds
+ * seq_lens[b] (>= 1).  The workspace holds the device error word, the work
+ * plan, the arrival counters of the fused merge and the split partials.
+ */
+int dcp_workspace_size(const dcp_params* params, int32_t B, int64_t max_seq_len, size_t* bytes);
+
+/* Zero a freshly allocated workspace (error word and counters).  Call once
+ * after allocation; later calls keep the workspace consistent themselves. */
+int dcp_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronize `stream`, read the device error word of `workspace` into *bits
+ * (0 = clean; DCP_DEV_ERR_* bits otherwise) and clear it.
+ */
+int dcp_get_error(void* workspace, cudaStream_t stream, uint32_t* bits);
+
+/*
+ * Token ownership, local lengths, virtual-block counts, slots and the cache
+ * write ("Breaking the Long-Sequence Inference Bottleneck ...", section 2:
+ * interleave rule, virtual block, slot mapping with -1 skip; "vLLM DCP and
+ * PCP", Deep Dive 5: local lengths).
+ *
+ * For the B requests (global lengths seq_lens[B]) writes, each output
+ * optional (NULL skips it):
+ *   local_lens[N][B]   tokens of request b owned by rank r
+ *   virt_blocks[B]     ceil(seq_lens[b] / (block_size * N))
+ *   rank_blocks[N][B]  ceil(local_lens[r][b] / block_size): physical blocks
+ *                      rank r needs for request b
+ * For the T tokens (tok_req[T], tok_pos[T]) writes:
+ *   owner[T]           owning rank floor(pos / I) mod N
+ *   slots[N][T]        owner's slot block_tables[r][b][lp / bs] * bs + lp % bs
+ *                      (lp = the token's local position: the number of earlier
+ *                      tokens of the request that the same rank owns), and -1
+ *                      in every other rank's row; needs block_tables
+ * and, when new_k != NULL (needs block_tables and k_pool), copies each
+ * token's row into its owner's slot: GQA new_k [T][Hkv][Dk] -> k_pool,
+ * new_v [T][Hkv][Dv] -> v_pool; MLA new_k [T][Dk] -> k_pool (new_v NULL).
+ * Rows are stored as given (kv_dtype; no requantisation).
+ * Device checks: token outside its request -> DCP_DEV_ERR_TOKEN; local block
+ * index >= max_blocks -> DCP_DEV_ERR_TABLE; block id outside
+ * [0, num_blocks) -> DCP_DEV_ERR_BLOCK_ID; the token's slots stay -1 and its
+ * row is not written.  The workspace needs at least dcp_workspace_size bytes
+ * for (params, B).
+ */
+int dcp_slot_mapping(const dcp_params* params, int32_t B, const int32_t* seq_lens,
+                     int64_t T, const int32_t* tok_req, const int64_t* tok_pos,
+                     const int32_t* block_tables, int32_t max_blocks, int64_t num_blocks,
+                     int8_t* owner, int64_t* slots, int32_t* local_lens,
+                     int32_t* virt_blocks, int32_t* rank_blocks,
+                     const void* new_k, const void* new_v, void* k_pool, void* v_pool,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Per-rank partial decode attention ("vLLM DCP and PCP", Deep Dive 6,
+ * "Deriving the partial and global outputs"): for every virtual rank r,
+ * request b, query token t and head h, with s_j = softmax_scale * q . k_j over
+ * the tokens j of rank r that query t may see (local positions
+ * < local_len_r(seq_lens[b] - Tq + t + 1)):
+ *   lse_partial = log sum_j exp(s_j),  out_partial = sum_j exp(s_j - lse) v_j.
+ * Inputs as in the layout notes above; local_lens must be the values
+ * dcp_slot_mapping gives for seq_lens (checked on device: DCP_DEV_ERR_STALE).
+ */
+int dcp_partial_attention(const dcp_params* params, int32_t B, const void* q,
+                          const void* k_pool, const void* v_pool, int64_t num_blocks,
+                          const int32_t* block_tables, int32_t max_blocks,
+                          const int32_t* seq_lens, const int32_t* local_lens,
+                          float* out_partial, float* lse_partial,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Exact LSE merge of N partials per row ("vLLM DCP and PCP", Deep Dive 6):
+ *   out_partial [N][rows][Dv] fp32, lse_partial [N][rows] fp32 (natural log)
+ *   -> out [rows][Dv] (out_dtype: DCP_F32 or DCP_BF16), lse [rows] fp32.
+ * Partials with lse = -inf carry no weight; a row whose partials are all
+ * -inf gives zeros and -inf.  lse may be NULL.
+ */
+int dcp_lse_merge(int32_t N, int64_t rows, int32_t Dv, const float* out_partial,
+                  const float* lse_partial, void* out, int32_t out_dtype, float* lse,
+                  cudaStream_t stream);
+
+/*
+ * Fused decode attention: the partial attention of every virtual rank and the
+ * exact LSE merge in one pass over the paged cache.  Same inputs as
+ * dcp_partial_attention; writes out [B][Tq][Hq][Dv] (out_dtype) and
+ * lse [B][Tq][Hq] fp32 (lse may be NULL).  Equal, up to fp32 rounding order,
+ * to dcp_partial_attention followed by dcp_lse_merge.
+ */
+int dcp_decode_attention(const dcp_params* params, int32_t B, const void* q,
+                         const void* k_pool, const void* v_pool, int64_t num_blocks,
+                         const int32_t* block_tables, int32_t max_blocks,
+                         const int32_t* seq_lens, const int32_t* local_lens,
+                         void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCP_H_ */

@@ -1,0 +1,196 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle, element
+by element, at sizes the oracle finishes in seconds that still span several
+chunks, splits and a ragged tail; plus the degenerate cases of the method."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dcp_workloads import config, make_workload
+
+from gpu_common import assert_close_rows, f64, tol_for
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "gqa_toy_fp32": config("gqa_toy"),
+    "gqa_bf16_ragged": config("gqa_llama8b", B=3, lengths=("list", [1000, 37, 513])),
+    "gqa_bf16_tq2": config("gqa_llama8b", B=2, Tq=2, lengths=("list", [301, 77])),
+    "gqa_bf16_tq3_rows24": config("gqa_llama8b", B=2, Tq=3, Hq=16, Hkv=2, lengths=("list", [100, 260])),
+    "gqa_bf16_bs8": config("gqa_llama8b", B=2, block_size=8, lengths=("list", [333, 64])),
+    "gqa_bf16_I64_short": config("gqa_llama8b", B=3, N=4, I=64, lengths=("list", [100, 700, 3])),
+    "gqa_bf16_N1": config("gqa_llama8b", B=2, N=1, lengths=("list", [257, 16])),
+    "gqa_bf16_single_token": config("gqa_llama8b", B=3, lengths=("list", [1, 1, 2])),
+    "gqa_bf16_d64": config("gqa_llama8b", B=2, Hq=8, Hkv=2, Dk=64, Dv=64, N=3, I=5, lengths=("list", [600, 91])),
+    "gqa_fp8": config("gqa_llama8b", B=2, kv_dtype="fp8", lengths=("list", [400, 129])),
+    "mla_bf16": config("mla_bf16_32k", B=2, lengths=("list", [700, 1531])),
+    "mla_bf16_I64_short": config("mla_bf16_32k", B=2, lengths=("list", [100, 64])),
+    "mla_fp8_mixed": config("mla_fp8_mixed", B=3, lengths=("list", [300, 1100, 77])),
+    "mla_fp8_tq4": config("mla_fp8_1m", lengths=("list", [2000])),
+}
+
+_cache = {}
+
+
+def _setup(name, seed=1):
+    key = (name, seed)
+    if key not in _cache:
+        from context_decode_attention_gb300.harness import DeviceWorkload
+        wl = make_workload(CASES[name], seed=seed)
+        dw = DeviceWorkload(wl)
+        _cache.clear()
+        _cache[key] = (wl, dw)
+    return _cache[key]
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_slot_mapping_and_cache_write_bit_exact(name):
+    wl, dw = _setup(name)
+    c = wl.cfg
+    N, I, bs = int(c["N"]), int(c["I"]), int(c["block_size"])
+    tok_req, tok_pos = wl.token_lists()
+    ref = oracle.slot_mapping(N, I, bs, wl.seq_lens, tok_req, tok_pos, dw.block_tables_host)
+    assert ref["status"] == 0
+    owner, slots = dw.slot_mapping(tok_req, tok_pos)
+    assert np.array_equal(owner.cpu().numpy(), ref["owner"])
+    assert np.array_equal(slots.cpu().numpy(), ref["slots"])
+    assert np.array_equal(dw.local_lens.cpu().numpy(), ref["local_lens"])
+    assert np.array_equal(dw.virt_blocks.cpu().numpy(), ref["virt_blocks"])
+    assert np.array_equal(dw.rank_blocks.cpu().numpy(), ref["rank_blocks"])
+    # every token's row sits, bit for bit, in its owner's slot
+    own_slot = ref["slots"][ref["owner"].astype(np.int64), np.arange(tok_req.size)]
+    blk, off = own_slot // bs, own_slot % bs
+    kp = dw.k_pool.view(torch.uint8).cpu().numpy() if dw.k_pool.dtype != torch.uint8 else dw.k_pool.cpu().numpy()
+    kraw = wl.k.view(np.uint8).reshape(wl.k.shape[0], wl.k.shape[1], -1)
+    if dw.mla:
+        got = kp.reshape(dw.num_blocks, bs, -1)[blk, off]
+        assert np.array_equal(got, kraw[:, 0])
+    else:
+        got = kp.reshape(dw.num_blocks, dw.Hkv, bs, -1)[blk, :, off]
+        assert np.array_equal(got, kraw)
+        vp = dw.v_pool.view(torch.uint8).cpu().numpy() if dw.v_pool.dtype != torch.uint8 else dw.v_pool.cpu().numpy()
+        vraw = wl.v.view(np.uint8).reshape(wl.v.shape[0], wl.v.shape[1], -1)
+        assert np.array_equal(vp.reshape(dw.num_blocks, dw.Hkv, bs, -1)[blk, :, off], vraw)
+    assert dw.error_bits() == 0
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_decode_attention_matches_oracle(name):
+    wl, dw = _setup(name)
+    out, lse = dw.decode()
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attention(wl)
+    assert_close_rows(f64(out).reshape(ref_o.shape), f64(lse).reshape(-1), ref_o, ref_l, tol_for(wl.cfg), name)
+    assert dw.error_bits() == 0
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_partial_attention_per_rank_matches_oracle(name):
+    wl, dw = _setup(name)
+    op, lp = dw.partial()
+    torch.cuda.synchronize()
+    N = int(wl.cfg["N"])
+    for r in range(N):
+        ref_o, ref_l = oracle.attention(wl, rank=r)
+        assert_close_rows(f64(op[r]).reshape(ref_o.shape), f64(lp[r]).reshape(-1), ref_o, ref_l,
+                          tol_for(wl.cfg), f"{name} rank {r}")
+    assert dw.error_bits() == 0
+
+
+@pytest.mark.parametrize("name", ["gqa_bf16_ragged", "gqa_bf16_I64_short", "mla_fp8_tq4", "gqa_toy_fp32"])
+def test_lse_merge_of_partials_matches_unsharded_oracle(name):
+    wl, dw = _setup(name)
+    dw.partial()
+    out = torch.empty_like(dw.out)
+    lse = torch.empty_like(dw.lse)
+    dw.merge(out, lse)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attention(wl)
+    assert_close_rows(f64(out).reshape(ref_o.shape), f64(lse).reshape(-1), ref_o, ref_l, tol_for(wl.cfg), name)
+
+
+def test_lse_merge_standalone_random_partials():
+    import context_decode_attention_gb300 as dcp
+    rng = np.random.default_rng(9)
+    N, rows, Dv = 5, 77, 96
+    o = rng.standard_normal((N, rows, Dv))
+    l = rng.standard_normal((N, rows)) * 3
+    l[1, :10] = -np.inf
+    l[:, 20] = -np.inf  # a row with no tokens at all
+    o[1, :10] = 0
+    o[:, 20] = 0
+    ref_o, ref_l = oracle.merge(o, l)
+    od = torch.from_numpy(o.astype(np.float32)).cuda()
+    ld = torch.from_numpy(l.astype(np.float32)).cuda()
+    for dt, torch_dt, tol in [(dcp.DCP_F32, torch.float32, (1e-5, 1e-5)), (dcp.DCP_BF16, torch.bfloat16, (2e-2, 1e-5))]:
+        out = torch.empty((rows, Dv), dtype=torch_dt, device="cuda")
+        lse = torch.empty(rows, dtype=torch.float32, device="cuda")
+        dcp.dcp_lse_merge(N, rows, Dv, od, ld, out, dt, lse)
+        torch.cuda.synchronize()
+        # the oracle merges the same fp32-rounded partials
+        ref_o, ref_l = oracle.merge(o.astype(np.float32).astype(np.float64), l.astype(np.float32).astype(np.float64))
+        assert_close_rows(f64(out), f64(lse), ref_o, ref_l, tol, "standalone merge")
+
+
+@pytest.mark.parametrize("name", ["gqa_bf16_ragged", "mla_fp8_tq4"])
+def test_decode_step_with_cache_write(name):
+    wl, dw = _setup(name)
+    out, lse = dw.step()
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attention(wl)
+    assert_close_rows(f64(out).reshape(ref_o.shape), f64(lse).reshape(-1), ref_o, ref_l, tol_for(wl.cfg), name)
+
+
+@pytest.mark.parametrize("seed", [2, 3])
+def test_decode_is_deterministic_and_seed_independent_of_layout(seed):
+    wl, dw = _setup("gqa_bf16_ragged", seed=seed)
+    a, la = dw.decode()
+    a = a.clone(); la = la.clone()
+    b, lb = dw.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+# ---------------------------------------------------------------- device errors
+
+def test_out_of_range_block_id_sets_error_bit():
+    import context_decode_attention_gb300 as dcp
+    wl, dw = _setup("gqa_bf16_ragged")
+    bt = dw.block_tables.clone()
+    bt[0, 0, 0] = dw.num_blocks + 5  # outside the pool: the kernels check before reading
+    dcp.dcp_decode_attention(dw.params, dw.q, dw.k_pool, dw.v_pool, dw.num_blocks, bt, dw.seq_lens,
+                             dw.local_lens, dw.out, dw.lse, dw.workspace)
+    assert dw.error_bits() & 0x1
+    assert dw.error_bits() == 0  # cleared by the read
+    owner = torch.empty(4, dtype=torch.int8, device="cuda")
+    slots = torch.empty((int(wl.cfg["N"]), 4), dtype=torch.int64, device="cuda")
+    req = torch.zeros(4, dtype=torch.int32, device="cuda")
+    pos = torch.arange(4, dtype=torch.int64, device="cuda")
+    dcp.dcp_slot_mapping(dw.params, dw.seq_lens, req, pos, bt, dw.num_blocks, owner=owner, slots=slots,
+                         workspace=dw.workspace)
+    assert dw.error_bits() & 0x1
+    assert (slots[:, 0] == -1).all()
+
+
+def test_stale_local_lengths_detected():
+    import context_decode_attention_gb300 as dcp
+    wl, dw = _setup("gqa_bf16_ragged")
+    stale = dw.local_lens.clone()
+    stale[1, 0] -= 1
+    dcp.dcp_decode_attention(dw.params, dw.q, dw.k_pool, dw.v_pool, dw.num_blocks, dw.block_tables, dw.seq_lens,
+                             stale, dw.out, dw.lse, dw.workspace)
+    assert dw.error_bits() & 0x8
+
+
+def test_token_outside_request_detected():
+    import context_decode_attention_gb300 as dcp
+    wl, dw = _setup("gqa_bf16_ragged")
+    owner = torch.empty(2, dtype=torch.int8, device="cuda")
+    slots = torch.empty((int(wl.cfg["N"]), 2), dtype=torch.int64, device="cuda")
+    req = torch.tensor([1, 7], dtype=torch.int32, device="cuda")      # request 7 does not exist
+    pos = torch.tensor([37, 0], dtype=torch.int64, device="cuda")     # request 1 has 37 tokens
+    dcp.dcp_slot_mapping(dw.params, dw.seq_lens, req, pos, dw.block_tables, dw.num_blocks, owner=owner,
+                         slots=slots, workspace=dw.workspace)
+    assert dw.error_bits() & 0x2
+    assert (slots == -1).all() and (owner == -1).all()
