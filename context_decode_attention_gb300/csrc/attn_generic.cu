@@ -24,7 +24,9 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(AttnArgs a, int q_dty
     const int64_t P = hdr->total_chunks;
     if (P == 0) return;
     const int64_t w = blockIdx.x;
-    const int64_t c0 = worker_begin(w, a.W, P), c1 = worker_begin(w + 1, a.W, P);
+    const int64_t We = P < a.W ? P : a.W;  // workers in play: each owns >= 1 chunk
+    if (w >= We) return;
+    const int64_t c0 = worker_begin(w, We, P), c1 = worker_begin(w + 1, We, P);
     if (c0 >= c1) return;
     const int64_t* unit_start = reinterpret_cast<const int64_t*>(a.ws + a.lay.off_units);
     const int32_t* seg_base = reinterpret_cast<const int32_t*>(a.ws + a.lay.off_seg_base);
@@ -52,7 +54,7 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(AttnArgs a, int q_dty
 
     auto flush = [&](int64_t group) {
         const int64_t first = unit_start[group * per_group];
-        const int64_t slot = seg_base[group] + (w - worker_of(first, a.W, P));
+        const int64_t slot = seg_base[group] + (w - worker_of(first, We, P));
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i) {
             const int row = my_rows[i];

@@ -81,7 +81,9 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(a.ws);
     const int64_t P = hdr->total_chunks;
     if (P == 0) return;
-    const int64_t c0 = worker_begin(w, a.W, P), c1 = worker_begin(w + 1, a.W, P);
+    const int64_t We = P < a.W ? P : a.W;  // workers in play: each owns >= 1 chunk
+    if (w >= We) return;
+    const int64_t c0 = worker_begin(w, We, P), c1 = worker_begin(w + 1, We, P);
     if (c0 >= c1) return;
     const int64_t* unit_start = reinterpret_cast<const int64_t*>(a.ws + a.lay.off_units);
     const int32_t* seg_base = reinterpret_cast<const int32_t*>(a.ws + a.lay.off_seg_base);
@@ -158,8 +160,8 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
         const float invA = (la > 0.f) ? 1.f / la : 0.f, invB = (lb > 0.f) ? 1.f / lb : 0.f;
         const int64_t first = unit_start[group * per_group];
         const int64_t last = unit_start[(group + 1) * per_group] - 1;
-        const int64_t wf = worker_of(first, a.W, P);
-        const int nseg = (int)(worker_of(last, a.W, P) - wf + 1);
+        const int64_t wf = worker_of(first, We, P);
+        const int nseg = (int)(worker_of(last, We, P) - wf + 1);
         const int b = cur_b, kvh = cur_kvh, r = cur_r;
         auto out_row = [&](int row) -> int64_t {
             const int t = row / a.G, gq = row % a.G;

@@ -90,7 +90,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (tid == 0) carry = 0;
     __syncthreads();
 
-    // 2. segments per merge group
+    // 2. segments per merge group.  With fewer chunks than workers only the
+    // first P workers take part, so every worker in play owns >= 1 chunk.
+    const int64_t We = P < a.W ? P : a.W;
     const int64_t per_group = a.partial_mode ? 1 : a.N;
     for (int64_t base = 0; base < a.G; base += kPlanThreads) {
         const int64_t g = base + tid;
@@ -98,7 +100,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         if (g < a.G) {
             const int64_t first = unit_start[g * per_group];
             const int64_t end = unit_start[(g + 1) * per_group];
-            if (end > first) cnt = worker_of(end - 1, a.W, P) - worker_of(first, a.W, P) + 1;
+            if (end > first) cnt = worker_of(end - 1, We, P) - worker_of(first, We, P) + 1;
             counters[g] = 0;
         }
         const int64_t incl = block_inclusive_scan(cnt, warp_tot);

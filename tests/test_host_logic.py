@@ -1,0 +1,56 @@
+"""Host-side logic of the work split, checked on the CPU.
+
+The attention kernels deal P chunks to We = min(W, P) workers as equal
+contiguous ranges [w P / We, (w + 1) P / We) and give each merge group one
+partial slot per worker that touches it.  These tests check the arithmetic the
+planner and kernels share (worker_of / worker_begin in dcp_internal.cuh): every
+worker in play owns at least one chunk, worker_of inverts the ranges, and the
+segment count of a group equals the number of distinct workers touching it,
+including when there are fewer chunks than workers.
+"""
+
+import numpy as np
+import pytest
+
+
+def worker_begin(w, W, P):
+    return w * P // W
+
+
+def worker_of(x, W, P):
+    return ((x + 1) * W - 1) // P
+
+
+@pytest.mark.parametrize("P,W", [(1, 1), (1, 1216), (7, 1216), (300, 1216), (1216, 1216), (131072, 1216),
+                                 (5, 3), (1000003, 608)])
+def test_ranges_cover_and_invert(P, W):
+    We = min(W, P)
+    starts = np.array([worker_begin(w, We, P) for w in range(We + 1)])
+    assert starts[0] == 0 and starts[-1] == P
+    assert np.all(np.diff(starts) >= 1)  # every worker in play owns >= 1 chunk
+    xs = np.unique(np.concatenate([np.arange(min(P, 2000)), np.random.default_rng(0).integers(0, P, 2000)]))
+    for x in xs:
+        w = worker_of(int(x), We, P)
+        assert starts[w] <= x < starts[w + 1]
+
+
+def test_segment_counts_match_distinct_workers():
+    rng = np.random.default_rng(1)
+    for trial in range(200):
+        groups = rng.integers(0, 6, size=rng.integers(1, 40))
+        P = int(groups.sum())
+        if P == 0:
+            continue
+        W = int(rng.integers(1, 3 * P + 5))
+        We = min(W, P)
+        bounds = np.concatenate([[0], np.cumsum(groups)])
+        total = 0
+        for g in range(len(groups)):
+            a, e = bounds[g], bounds[g + 1]
+            if e == a:
+                continue
+            cnt = worker_of(int(e - 1), We, P) - worker_of(int(a), We, P) + 1
+            owners = {worker_of(int(x), We, P) for x in range(a, e)}
+            assert cnt == len(owners)
+            total += cnt
+        assert total <= We + len(groups)
