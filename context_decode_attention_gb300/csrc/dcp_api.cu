@@ -50,11 +50,12 @@ int validate_params(const dcp_params* p) {
 
 bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15) == 0; }
 
-enum class Kernel { kNone, kGeneric, kGqaMma };
+enum class Kernel { kNone, kGeneric, kGqaMma, kMlaTc };
 
 const char* kernel_name(Kernel k) {
     switch (k) {
         case Kernel::kGqaMma: return "gqa_mma";
+        case Kernel::kMlaTc: return "mla_tcgen05";
         case Kernel::kGeneric: return "generic";
         default: return nullptr;
     }
@@ -62,13 +63,15 @@ const char* kernel_name(Kernel k) {
 
 Kernel select_kernel(const dcp_params& p) {
     if (gqa_mma_supported(p)) return Kernel::kGqaMma;
+    if (mla_tc_supported(p)) return Kernel::kMlaTc;
     if (generic_supported(p)) return Kernel::kGeneric;
     return Kernel::kNone;
 }
 
-int64_t kernel_workers(Kernel k, int sms) {
+int64_t kernel_workers(Kernel k, int sms, const dcp_params& p) {
     switch (k) {
         case Kernel::kGqaMma: return gqa_mma_workers(sms);
+        case Kernel::kMlaTc: return mla_tc_workers(sms, p.Tq);
         case Kernel::kGeneric: return generic_workers(sms);
         default: return 0;
     }
@@ -77,6 +80,7 @@ int64_t kernel_workers(Kernel k, int sms) {
 int kernel_chunk(Kernel k, const dcp_params& p) {
     switch (k) {
         case Kernel::kGqaMma: return 16;
+        case Kernel::kMlaTc: return 64;
         case Kernel::kGeneric: return generic_chunk(p.block_size);
         default: return 1;
     }
@@ -88,7 +92,7 @@ bool layout_for(const dcp_params& p, int32_t B, WsLayout* out, Kernel* kout, int
     if (sms <= 0) return false;
     const Kernel k = select_kernel(p);
     const int64_t U = (int64_t)B * p.Hkv * p.N;
-    const int64_t w = k == Kernel::kNone ? 0 : kernel_workers(k, sms);
+    const int64_t w = k == Kernel::kNone ? 0 : kernel_workers(k, sms, p);
     const int64_t rows = (int64_t)p.Tq * (p.Hq / p.Hkv);
     *out = ws_layout(U, U, w + U, rows, p.Dv);
     if (kout) *kout = k;
@@ -148,6 +152,13 @@ int run_attention(const dcp_params* params, int32_t B, const void* q, const void
     if (kern == Kernel::kGqaMma) {
         e = launch_attn_gqa_mma(a, stream);
         count_launches(1);
+    } else if (kern == Kernel::kMlaTc) {
+        e = launch_attn_mla_tc(a, p.kv_dtype, stream);
+        count_launches(1);
+        if (e == cudaSuccess && a.Gn > 0) {
+            e = launch_segment_merge(a, stream);
+            count_launches(1);
+        }
     } else {
         e = launch_attn_generic(a, p.q_dtype, p.kv_dtype, stream);
         count_launches(1);

@@ -145,6 +145,12 @@ bool gqa_mma_supported(const dcp_params& p);
 int64_t gqa_mma_workers(int num_sms);
 cudaError_t launch_attn_gqa_mma(const AttnArgs& a, cudaStream_t s);
 
+// MLA (128 heads, 576/512 latent, bf16 or fp8 cache) on tcgen05; writes
+// segment partials, then launch_segment_merge combines them.
+bool mla_tc_supported(const dcp_params& p);
+int64_t mla_tc_workers(int num_sms, int Tq);
+cudaError_t launch_attn_mla_tc(const AttnArgs& a, int kv_dtype, cudaStream_t s);
+
 // standalone merge for dcp_lse_merge
 cudaError_t launch_lse_merge(int N, int64_t rows, int Dv, const float* o_parts, const float* lse_parts,
                              void* out, int out_dtype, float* lse, cudaStream_t s);

@@ -50,6 +50,9 @@
  *  - out_partial [N][B][Tq][Hq][Dv] fp32;  lse_partial [N][B][Tq][Hq] fp32;
  *                a rank with no visible token gives zeros and -inf.
  *  - GQA head mapping: query head h reads KV head h / (Hq / Hkv).
+ *  - Slots of a rank's last block past its local length must hold finite
+ *    values (a zero-initialised pool, or slots written earlier): the tensor-
+ *    core kernels read whole 16/64-token tiles and weight those slots by 0.
  */
 #ifndef DCP_H_
 #define DCP_H_

@@ -120,3 +120,13 @@ def test_slot_mapping_argument_rules(libdcp):
     rc = libdcp.dcp_slot_mapping(ctypes.byref(p), 2, dummy, 0, None, None, None, 0, 0, None, None, dummy,
                                  None, None, None, None, None, None, dummy, 16, None)
     assert rc == 4
+
+
+@pytest.mark.parametrize("name,kernel", [
+    ("gqa_toy", "generic"), ("gqa_llama8b", "gqa_mma"), ("mla_bf16_32k", "mla_tcgen05"),
+    ("mla_fp8_mixed", "mla_tcgen05"), ("mla_fp8_1m", "mla_tcgen05"),
+])
+def test_each_workload_selects_its_kernel(libdcp, name, kernel):
+    from context_decode_attention_gb300 import dcp_attention_kernel, params_from_config
+    from dcp_workloads import config
+    assert dcp_attention_kernel(params_from_config(config(name), kv_scale=0.01 if "fp8" in name else 1.0)) == kernel
