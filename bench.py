@@ -220,6 +220,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling a smaller case)")
+    ap.add_argument("--context", type=int, default=0, help="override to one fixed context length")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
@@ -235,7 +237,12 @@ def main():
         dist.init_process_group("gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = config(args.workload)
+    over = {}
+    if args.batch:
+        over["B"] = args.batch
+    if args.context:
+        over["L"] = args.context
+    cfg = config(args.workload, **over)
     wl = make_workload(cfg, seed=int(cfg["index"]) + 1000 * rank)  # replicas: same shape, own data
     dw = DeviceWorkload(wl, device=dev)
     stream = dw.stream

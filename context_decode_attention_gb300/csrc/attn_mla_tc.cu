@@ -16,11 +16,13 @@
 // the range itself.  A tile is up to two 64-token chunks (one TMA box each);
 // K and V stream through a ring of [tile x 64-column] sub-tiles.
 //
-// Warp roles (per CTA):
-//   warp 0        TMA producer (one lane)
-//   warp 1        TMEM owner and MMA issuer (one lane)
-//   warps 2-5     softmax / O correction / segment epilogue; thread = head
-//   warps 6-9     (fp8 cache only) fp8 -> fp16 converters
+// Warp roles (per CTA), bf16 cache:
+//   warps 0-3     TMA producers: warp p owns ring slot p (one TMA instruction
+//                 occupies its issuing warp for ~440 cycles, so issue is spread)
+//   warp 4        TMEM owner and MMA issuer (one lane)
+//   warps 5-8     softmax / O correction / segment epilogue; thread = head
+// fp8 cache: warp 0 TMA producer into the fp8 staging ring, warp 1 MMA,
+//   warps 2-5 softmax, warps 6-9 fp8 -> fp16 converters.
 // TMEM: O half [0, 256), S double buffer [256, 384) and [384, 512); P is
 // written back as 16-bit pairs over the first columns of its S buffer and read
 // by the P.V MMA straight from TMEM.
@@ -48,12 +50,17 @@ constexpr int kQBytes = kHeads * kDk * 2;    // 147456
 constexpr int kSubBytes = 2 * kChunk * 128;  // [128 rows x 64 cols] 16-bit, SW128: 16384
 constexpr float kRescaleLog2 = 8.f;
 
+constexpr int kProd = 4;  // TMA issuing warps (one TMA per ~440 cycles per warp)
+
 template <bool FP8>
 struct MlaCfg {
     static constexpr int kRing = FP8 ? 3 : 4;
     static constexpr int kStage = FP8 ? 4 : 0;          // fp8 staging slots
     static constexpr int kStageBytes = 2 * kChunk * 64;  // [128 rows x 64 fp8]
-    static constexpr int kThreads = FP8 ? 320 : 192;
+    static constexpr int kWarpMma = FP8 ? 1 : kProd;     // TMEM owner / MMA issuer
+    static constexpr int kWarpSoftmax = kWarpMma + 1;     // 4 softmax warps
+    static constexpr int kWarpConv = kWarpSoftmax + 4;    // fp8: 4 converter warps
+    static constexpr int kThreads = 32 * (FP8 ? kWarpConv + 4 : kWarpSoftmax + 4);
     static constexpr int kOffQ = 0;
     static constexpr int kOffRing = kQBytes;
     static constexpr int kOffStage = kOffRing + kRing * kSubBytes;
@@ -192,7 +199,7 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_kv);
     }
-    if (warp == 1) {
+    if (warp == C::kWarpMma) {
         tmem_alloc(sh.tmem_slot, 512);
         tmem_relinquish();
     }
@@ -203,37 +210,64 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
     const uint32_t tm_o = tm;
     const int per_group = a.partial_mode ? 1 : a.N;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp < (FP8 ? 1 : kProd)) {
+        // ------------------------------------------------------------ TMA producers
+        // The ring items (K sub-tiles of tile t, then V sub-tiles of tile t-1)
+        // are numbered in consumption order; item k goes to ring slot k % kRing
+        // and is issued by producer warp k % nprod.  Block ids are read once per
+        // tile, one tile ahead of their use.
         if (lane == 0) {
+            const int nprod = FP8 ? 1 : kProd;
+            const int me = warp;
             TileCursor cur;
             cur.init(us, c0, c1, u0, a.N, a.partial_mode);
             Ring ring;
             ring.n = FP8 ? C::kStage : C::kRing;
             uint32_t qe_phase = 0;
             bool alive = true, bad_block = false;
-            MlaTile prev{}, t{};
-            int ti = 0;
-            auto load_sub = [&](const MlaTile& tt, int col) {
-                uint64_t* fullb = FP8 ? &sh.sfull[ring.slot] : &sh.full[ring.slot];
-                uint64_t* emptyb = FP8 ? &sh.sempty[ring.slot] : &sh.empty[ring.slot];
-                if (!mbar_wait(emptyb, ring.phase ^ 1u)) { alive = false; return; }
-                const int box_bytes = FP8 ? kChunk * 64 : kChunk * 128;
-                mbar_arrive_expect_tx(fullb, (uint32_t)(box_bytes * tt.n_ch));
-                uint8_t* dst = FP8 ? sStage + ring.slot * C::kStageBytes : sRing + ring.slot * kSubBytes;
-                const int r = (int)(tt.u % a.N), b = (int)(tt.u / a.N);
-                for (int k = 0; k < tt.n_ch; ++k) {
-                    const int64_t p = (tt.chunk + k) * kChunk;
-                    int32_t blk = a.block_tables[((int64_t)r * a.B + b) * a.max_blocks + p / a.bs];
-                    if (blk < 0 || blk >= a.num_blocks) { bad_block = true; blk = 0; }
-                    tma_load_2d(dst + k * box_bytes, &tmap_kv, col, (int)((int64_t)blk * a.bs + p % a.bs), fullb);
+            struct Ahead {
+                MlaTile t;
+                int32_t blk[2];
+                bool valid;
+            };
+            auto fetch = [&](Ahead& x) {
+                x.valid = cur.next(x.t);
+                if (!x.valid) return;
+                const int r = (int)(x.t.u % a.N), b = (int)(x.t.u / a.N);
+                const int32_t* bt = a.block_tables + ((int64_t)r * a.B + b) * a.max_blocks;
+                for (int k = 0; k < 2; ++k)
+                    x.blk[k] = (k < x.t.n_ch) ? bt[((x.t.chunk + k) * kChunk) / a.bs] : 0;
+            };
+            auto row_of = [&](const Ahead& x, int k) -> int {
+                int32_t blk = x.blk[k];
+                if (blk < 0 || blk >= a.num_blocks) { bad_block = true; blk = 0; }
+                const int64_t p = (x.t.chunk + k) * kChunk;
+                return (int)((int64_t)blk * a.bs + p % a.bs);
+            };
+            int64_t item = 0;  // global item index in consumption order
+            auto load_sub = [&](const Ahead& x, int col) {
+                if ((int)(item % nprod) == me) {
+                    uint64_t* fullb = FP8 ? &sh.sfull[ring.slot] : &sh.full[ring.slot];
+                    uint64_t* emptyb = FP8 ? &sh.sempty[ring.slot] : &sh.empty[ring.slot];
+                    if (!mbar_wait(emptyb, ring.phase ^ 1u)) { alive = false; return; }
+                    const int box_bytes = FP8 ? kChunk * 64 : kChunk * 128;
+                    mbar_arrive_expect_tx(fullb, (uint32_t)(box_bytes * x.t.n_ch));
+                    uint8_t* dst = FP8 ? sStage + ring.slot * C::kStageBytes : sRing + ring.slot * kSubBytes;
+                    for (int k = 0; k < x.t.n_ch; ++k)
+                        tma_load_2d(dst + k * box_bytes, &tmap_kv, col, row_of(x, k), fullb);
                 }
+                ++item;
                 ring.advance();
             };
+            Ahead cur_t, nxt, prev;
+            prev.valid = false;
+            fetch(cur_t);
+            int ti = 0;
             for (;;) {
-                const bool more = cur.next(t);
-                if (more) {
-                    if (t.first) {
+                fetch(nxt);  // next tile's block ids load while this tile's TMAs go out
+                if (cur_t.valid) {
+                    const MlaTile& t = cur_t.t;
+                    if (t.first && me == 0) {
                         if (ti > 0) {
                             if (!mbar_wait(sh.q_empty, qe_phase)) { alive = false; break; }
                             qe_phase ^= 1u;
@@ -243,18 +277,19 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
                         mbar_arrive_expect_tx(sh.q_full, kQBytes);
                         for (int j = 0; j < kKSub; ++j) tma_load_2d(sQ + j * 16384, &tmap_q, 64 * j, row0, sh.q_full);
                     }
-                    for (int s = 0; s < kKSub && alive; ++s) load_sub(t, 64 * s);
+                    for (int s2 = 0; s2 < kKSub && alive; ++s2) load_sub(cur_t, 64 * s2);
                 }
-                if (ti > 0)
+                if (prev.valid)
                     for (int j = 0; j < kVSub && alive; ++j) load_sub(prev, kDvHalf * half + 64 * j);
-                if (!more || !alive) break;
-                prev = t;
+                if (!cur_t.valid || !alive) break;
+                prev = cur_t;
+                cur_t = nxt;
                 ++ti;
             }
             if (bad_block) raise_err(err, DCP_DEV_ERR_BLOCK_ID);
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
         }
-    } else if (warp == 1) {
+    } else if (warp == C::kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             TileCursor cur;
@@ -320,7 +355,7 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
             }
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
         }
-    } else if (warp < 6) {
+    } else if (warp < C::kWarpSoftmax + 4) {
         // ------------------------------------------------------------ softmax warpgroup
         const int quarter = warp & 3;
         const int h = 32 * quarter + lane;  // head row = TMEM lane
@@ -414,7 +449,7 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
                     m_ref = mx;  // first visible tokens of the segment: O not yet accumulated
                     corr = 0.f;
                 } else if (mx > m_ref + kRescaleLog2) {
-                    corr = exp2f(m_ref - mx);
+                    corr = ex2_approx(m_ref - mx);
                     m_ref = mx;
                     rescale_o = true;
                 }
@@ -427,8 +462,8 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
                 if (cch * 64 < ncols) {
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        const float p_lo = exp2f(x[64 * cch + 2 * k] - mu);
-                        const float p_hi = exp2f(x[64 * cch + 2 * k + 1] - mu);
+                        const float p_lo = ex2_approx(x[64 * cch + 2 * k] - mu);
+                        const float p_hi = ex2_approx(x[64 * cch + 2 * k + 1] - mu);
                         lsum += p_lo + p_hi;
                         pk[k] = pack16(p_lo, p_hi, FP8);
                     }
@@ -465,7 +500,7 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
         if (!alive && lane == 0) raise_err(err, DCP_DEV_ERR_TIMEOUT);
     } else if (FP8) {
         // ------------------------------------------------------------ fp8 -> fp16 converters
-        const int ct = threadIdx.x - 192;  // 0..127
+        const int ct = threadIdx.x - 32 * C::kWarpConv;  // 0..127
         TileCursor cur;
         cur.init(us, c0, c1, u0, a.N, a.partial_mode);
         Ring stg, ring;
@@ -547,7 +582,7 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tm, 512);
+    if (warp == C::kWarpMma) tmem_dealloc(tm, 512);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
