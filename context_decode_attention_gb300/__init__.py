@@ -21,7 +21,8 @@ from ._lib import (
 __all__ = [
     "DcpError", "DcpParams", "params_from_config", "lib", "lib_path",
     "dcp_workspace_size", "dcp_workspace_init", "dcp_get_error", "dcp_slot_mapping",
-    "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention", "dcp_launch_count",
+    "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention", "dcp_decode_attention_noalloc",
+    "dcp_launch_count",
     "dcp_attention_kernel", "DCP_F32", "DCP_BF16", "DCP_FP8_E4M3", "DCP_LAYOUT_GQA", "DCP_LAYOUT_MLA",
 ]
 
@@ -124,3 +125,17 @@ def dcp_decode_attention(params, q, k_pool, v_pool, num_blocks, block_tables, se
 def dcp_lse_merge(N, rows, Dv, out_partial, lse_partial, out, out_dtype, lse=None, stream=None):
     _check(lib().dcp_lse_merge(int(N), int(rows), int(Dv), _ptr(out_partial), _ptr(lse_partial), _ptr(out),
                                int(out_dtype), _ptr(lse), _stream(stream)), "dcp_lse_merge")
+
+
+def dcp_decode_attention_noalloc(params, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens,
+                                 out, lse, stream=None):
+    """dcp_decode_attention on the library's static scratch (no workspace argument).
+
+    For callers that cannot allocate device memory; calls must not overlap on
+    the GPU (they share one scratch buffer).  See include/dcp.h.
+    """
+    _check(lib().dcp_decode_attention_noalloc(ctypes.byref(params), int(seq_lens.numel()), _ptr(q), _ptr(k_pool),
+                                              _ptr(v_pool), int(num_blocks), _ptr(block_tables),
+                                              int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(local_lens),
+                                              _ptr(out), _ptr(lse), _stream(stream)),
+           "dcp_decode_attention_noalloc")

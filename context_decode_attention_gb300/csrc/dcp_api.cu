@@ -285,3 +285,61 @@ int dcp_lse_merge(int32_t N, int64_t rows, int32_t Dv, const float* out_partial,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode attention with library-owned scratch, for callers that cannot
+// allocate device memory.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace dcp {
+namespace {
+
+constexpr size_t kStaticScratchBytes = DCP_STATIC_SCRATCH_BYTES;
+
+// One copy per device that loads this library, held until the process exits.
+// Host code must not use this name as a device address: it only stands in
+// for the symbol; static_scratch() looks up the device address.
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void* g_static_ptr[64] = {nullptr};
+
+// Device address of g_static_scratch on the current device (looked up once
+// per device, with that device current).  nullptr on failure.
+void* static_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return nullptr;
+        g_static_ptr[dev] = p;
+    }
+    return g_static_ptr[dev];
+}
+
+}  // namespace
+}  // namespace dcp
+
+extern "C" int dcp_decode_attention_noalloc(const dcp_params* params, int32_t B, const void* q,
+                                            const void* k_pool, const void* v_pool, int64_t num_blocks,
+                                            const int32_t* block_tables, int32_t max_blocks,
+                                            const int32_t* seq_lens, const int32_t* local_lens, void* out,
+                                            float* lse, cudaStream_t stream) {
+    int rc = validate_params(params);
+    if (rc != DCP_OK) return rc;
+    if (B < 0) return DCP_ERR_INVALID_ARG;
+    if (B == 0) return DCP_OK;
+    size_t need = 0;
+    rc = dcp_workspace_size(params, B, 1, &need);
+    if (rc != DCP_OK) return rc;
+    if (need > kStaticScratchBytes) return DCP_ERR_WORKSPACE;  // problem too large for the static scratch
+    void* ws = static_scratch();
+    if (ws == nullptr) return DCP_ERR_CUDA;
+    // the error word is the only scratch that must start at zero here: the
+    // planner resets the arrival counters and rewrites the plan every call
+    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), stream) != cudaSuccess) return DCP_ERR_CUDA;
+    return run_attention(params, B, q, k_pool, v_pool, num_blocks, block_tables, max_blocks, seq_lens, local_lens,
+                         false, nullptr, nullptr, out, lse, ws, kStaticScratchBytes, stream);
+}

@@ -211,6 +211,35 @@ int dcp_decode_attention(const dcp_params* params, int32_t B, const void* q,
                          void* out, float* lse,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Decode attention for callers that cannot allocate device memory.
+ *
+ * No passage of the pages has a counterpart to this call: it exists for
+ * callers that may not call cudaMalloc (or any allocator) when they run
+ * attention -- for example code enqueued while a framework captures a stream,
+ * or a plugin inside an engine that owns all device memory.  It computes
+ * exactly what dcp_decode_attention computes, with the same arguments minus
+ * the workspace: the scratch is a buffer of DCP_STATIC_SCRATCH_BYTES that
+ * this library declares as a static device array.  Every device that loads
+ * the library holds one such buffer until the process exits.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *  - The first call on a device looks up the buffer's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Returns DCP_ERR_WORKSPACE, without enqueuing work, when the problem
+ *    needs more scratch than the buffer holds (dcp_workspace_size tells).
+ *  - All calls share the one buffer and it keeps the last call's contents:
+ *    calls that overlap on the GPU (other streams, other host threads) race
+ *    and corrupt each other's results; serialize them.
+ *  - Device-side checks still run, but their error bits stay in the shared
+ *    buffer (cleared at the start of each call) and are not reported.
+ */
+#define DCP_STATIC_SCRATCH_BYTES (64u << 20)
+int dcp_decode_attention_noalloc(const dcp_params* params, int32_t B, const void* q,
+                                 const void* k_pool, const void* v_pool, int64_t num_blocks,
+                                 const int32_t* block_tables, int32_t max_blocks,
+                                 const int32_t* seq_lens, const int32_t* local_lens,
+                                 void* out, float* lse, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
