@@ -17,12 +17,13 @@
 // K and V stream through a ring of [tile x 64-column] sub-tiles.
 //
 // Warp roles (per CTA), bf16 cache:
-//   warps 0-3     TMA producers: warp p owns ring slot p (one TMA instruction
-//                 occupies its issuing warp for ~440 cycles, so issue is spread)
-//   warp 4        TMEM owner and MMA issuer (one lane)
-//   warps 5-8     softmax / O correction / segment epilogue; thread = head
-// fp8 cache: warp 0 TMA producer into the fp8 staging ring, warp 1 MMA,
-//   warps 2-5 softmax, warps 6-9 fp8 -> fp16 converters.
+//   warps 0-2     TMA producers: ring item k is issued by warp k % 3 (one TMA
+//                 instruction occupies its issuing warp for ~440 cycles)
+//   warp 3        TMEM owner and MMA issuer (one lane)
+//   warps 4-7     softmax / O correction / segment epilogue; thread = head
+// fp8 cache: the same, with the producers filling an fp8 staging ring and
+//   warps 8-11 converting it to fp16 into the MMA ring (12 warps, so the
+//   register limit is 168).
 // TMEM: O half [0, 256), S double buffer [256, 384) and [384, 512); P is
 // written back as 16-bit pairs over the first columns of its S buffer and read
 // by the P.V MMA straight from TMEM.
@@ -50,14 +51,22 @@ constexpr int kQBytes = kHeads * kDk * 2;    // 147456
 constexpr int kSubBytes = 2 * kChunk * 128;  // [128 rows x 64 cols] 16-bit, SW128: 16384
 constexpr float kRescaleLog2 = 8.f;
 
-constexpr int kProd = 4;  // TMA issuing warps (one TMA per ~440 cycles per warp)
+// TMA issuing warps (one TMA instruction per ~440 cycles per warp).  Three keep
+// the bf16 CTA at 8 warps: each of the four SM sub-partitions then hosts two
+// warps and the softmax warps can hold 255 registers (the register file is
+// split per sub-partition, 16K registers each).
+constexpr int kProd = 3;
 
 template <bool FP8>
 struct MlaCfg {
-    static constexpr int kRing = FP8 ? 3 : 4;
+    // bf16: a 5-slot ring; every tile's items are K (9), padding no-ops, then
+    // the previous tile's 4 V sub-tiles, which therefore always sit in slots
+    // 1-4, contiguous, so P.V runs as N = 256 MMAs.  fp8: 3-slot ring, N = 64.
+    static constexpr bool kWideV = !FP8;
+    static constexpr int kRing = FP8 ? 3 : 5;
     static constexpr int kStage = FP8 ? 4 : 0;          // fp8 staging slots
     static constexpr int kStageBytes = 2 * kChunk * 64;  // [128 rows x 64 fp8]
-    static constexpr int kWarpMma = FP8 ? 1 : kProd;     // TMEM owner / MMA issuer
+    static constexpr int kWarpMma = kProd;                 // TMEM owner / MMA issuer
     static constexpr int kWarpSoftmax = kWarpMma + 1;     // 4 softmax warps
     static constexpr int kWarpConv = kWarpSoftmax + 4;    // fp8: 4 converter warps
     static constexpr int kThreads = 32 * (FP8 ? kWarpConv + 4 : kWarpSoftmax + 4);
@@ -210,14 +219,14 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
     const uint32_t tm_o = tm;
     const int per_group = a.partial_mode ? 1 : a.N;
 
-    if (warp < (FP8 ? 1 : kProd)) {
+    if (warp < kProd) {
         // ------------------------------------------------------------ TMA producers
         // The ring items (K sub-tiles of tile t, then V sub-tiles of tile t-1)
         // are numbered in consumption order; item k goes to ring slot k % kRing
         // and is issued by producer warp k % nprod.  Block ids are read once per
         // tile, one tile ahead of their use.
         if (lane == 0) {
-            const int nprod = FP8 ? 1 : kProd;
+            const int nprod = kProd;
             const int me = warp;
             TileCursor cur;
             cur.init(us, c0, c1, u0, a.N, a.partial_mode);
@@ -245,6 +254,17 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
                 return (int)((int64_t)blk * a.bs + p % a.bs);
             };
             int64_t item = 0;  // global item index in consumption order
+            // a no-op item: keeps the ring aligned (the MMA warp just releases it)
+            auto pad_item = [&]() {
+                if ((int)(item % nprod) == me) {
+                    uint64_t* fullb = FP8 ? &sh.sfull[ring.slot] : &sh.full[ring.slot];
+                    uint64_t* emptyb = FP8 ? &sh.sempty[ring.slot] : &sh.empty[ring.slot];
+                    if (!mbar_wait(emptyb, ring.phase ^ 1u)) { alive = false; return; }
+                    mbar_arrive(fullb);
+                }
+                ++item;
+                ring.advance();
+            };
             auto load_sub = [&](const Ahead& x, int col) {
                 if ((int)(item % nprod) == me) {
                     uint64_t* fullb = FP8 ? &sh.sfull[ring.slot] : &sh.full[ring.slot];
@@ -278,6 +298,11 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
                         for (int j = 0; j < kKSub; ++j) tma_load_2d(sQ + j * 16384, &tmap_q, 64 * j, row0, sh.q_full);
                     }
                     for (int s2 = 0; s2 < kKSub && alive; ++s2) load_sub(cur_t, 64 * s2);
+                }
+                if (C::kWideV) {
+                    // V of the previous tile into slots 1..4; otherwise realign to slot 0
+                    const uint32_t target = prev.valid ? 1u : 0u;
+                    while (alive && ring.slot != target) pad_item();
                 }
                 if (prev.valid)
                     for (int j = 0; j < kVSub && alive; ++j) load_sub(prev, kDvHalf * half + 64 * j);
@@ -329,7 +354,37 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
                     mma_commit(&sh.s_full[sb]);
                     if (t.last) mma_commit(sh.q_empty);
                 }
-                if (ti > 0) {
+                if (C::kWideV) {
+                    // consume the padding items that realign the ring
+                    const uint32_t target = (ti > 0) ? 1u : 0u;
+                    while (ring.slot != target) {
+                        if (!mbar_wait(&sh.full[ring.slot], ring.phase)) { alive = false; break; }
+                        mbar_arrive(&sh.empty[ring.slot]);
+                        ring.advance();
+                    }
+                    if (!alive) break;
+                }
+                if (ti > 0 && C::kWideV) {
+                    // O[:, 0:256] += P V with V's four 64-column blocks in slots 1..4
+                    const int sb = (ti - 1) & 1;
+                    if (!mbar_wait(&sh.p_full[sb], pf_phase[sb])) { alive = false; break; }
+                    pf_phase[sb] ^= 1u;
+                    for (int j = 0; j < kVSub; ++j)
+                        if (!mbar_wait(&sh.full[1 + j], ring.phase)) { alive = false; break; }
+                    if (!alive) break;
+                    tc_fence_after();
+                    const uint32_t pa = tm + 256 + 128 * sb;
+                    const uint32_t vb = smem_u32(sRing + 1 * kSubBytes);
+                    const uint32_t idesc_pv256 = idesc_f16(ab, 128, 256, 0, 1);
+                    for (int kk = 0; kk < 4 * prev.n_ch; ++kk)
+                        mma_ts(tm_o, pa + 8 * kk, smem_desc(vb + kk * 2048, kSubBytes, 1024, kLayoutSW128), idesc_pv256,
+                               !(prev.first && kk == 0));
+                    for (int j = 0; j < kVSub; ++j) {
+                        mma_commit(&sh.empty[ring.slot]);
+                        ring.advance();
+                    }
+                    mma_commit(sh.o_done);
+                } else if (ti > 0) {
                     const int sb = (ti - 1) & 1;
                     if (!mbar_wait(&sh.p_full[sb], pf_phase[sb])) { alive = false; break; }
                     pf_phase[sb] ^= 1u;
@@ -421,26 +476,32 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
             const int64_t p0 = t.chunk * kChunk;
             const uint32_t sbase = tm + 256 + 128 * sb + lane_off;
             const int ncols = 64 * t.n_ch;
-            float x[128];
+            // columns [0, lim) are visible to this query token
+            const int64_t lim64 = bound - p0;
+            const int lim = lim64 <= 0 ? 0 : (lim64 >= ncols ? ncols : (int)lim64);
+            float sv[128];
             uint32_t rr[32];
-            float mx = -INFINITY;
 #pragma unroll
             for (int cch = 0; cch < 4; ++cch) {
                 if (cch * 32 < ncols) {
                     tmem_ld32(sbase + 32 * cch, rr);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int j = 32 * cch + k;
-                        const float v = (p0 + j < bound) ? __uint_as_float(rr[k]) * sl2 : -INFINITY;
-                        x[j] = v;
-                        mx = fmaxf(mx, v);
-                    }
+                    for (int k = 0; k < 32; ++k) sv[32 * cch + k] = __uint_as_float(rr[k]);
                 } else {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) x[32 * cch + k] = -INFINITY;
+                    for (int k = 0; k < 32; ++k) sv[32 * cch + k] = 0.f;
                 }
             }
+            float mraw = -INFINITY;
+            if (lim == 128) {
+#pragma unroll
+                for (int j = 0; j < 128; ++j) mraw = fmaxf(mraw, sv[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 128; ++j) mraw = (j < lim) ? fmaxf(mraw, sv[j]) : mraw;
+            }
+            const float mx = (lim > 0) ? mraw * sl2 : -INFINITY;
             // lazy reference max
             float corr = 1.f;
             bool rescale_o = false;
@@ -454,7 +515,7 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
                     rescale_o = true;
                 }
             }
-            const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+            const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
             float lsum = 0.f;
             uint32_t pk[32];
 #pragma unroll
@@ -462,8 +523,13 @@ __global__ void __launch_bounds__(MlaCfg<FP8>::kThreads, 1)
                 if (cch * 64 < ncols) {
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        const float p_lo = ex2_approx(x[64 * cch + 2 * k] - mu);
-                        const float p_hi = ex2_approx(x[64 * cch + 2 * k + 1] - mu);
+                        const int j = 64 * cch + 2 * k;
+                        float p_lo = ex2_approx(fmaf(sv[j], sl2, nmu));
+                        float p_hi = ex2_approx(fmaf(sv[j + 1], sl2, nmu));
+                        if (lim < 128) {
+                            p_lo = (j < lim) ? p_lo : 0.f;
+                            p_hi = (j + 1 < lim) ? p_hi : 0.f;
+                        }
                         lsum += p_lo + p_hi;
                         pk[k] = pack16(p_lo, p_hi, FP8);
                     }

@@ -79,6 +79,14 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int c0,
                  : "memory");
 }
 
+// Prefetch one 3D box into L2.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // 2^x on the SFU (ex2.approx.ftz: ~2 ulp; -inf -> +0).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
