@@ -20,6 +20,7 @@
 //    partial slot; the last arriving segment of a group merges the group's
 //    partials (atomic counter, no waiting).
 #include "dcp_internal.cuh"
+#include "sm100_prims.cuh"
 
 namespace dcp {
 namespace {
@@ -103,18 +104,32 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
         if (unit_start[mid] <= c0) lo = mid; else hi = mid - 1;
     }
     int64_t u_load = lo, u = lo;
+    // producer-side cache of the current unit (divisions only when the unit changes)
+    int64_t ld_start = unit_start[u_load], ld_end = unit_start[u_load + 1];
+    const int32_t* ld_bt = nullptr;
+    int ld_kvh = 0;
+    auto ld_unit = [&]() {
+        const int r = (int)(u_load % a.N);
+        const int64_t bk = u_load / a.N;
+        const int b = (int)(bk / a.Hkv);
+        ld_kvh = (int)(bk % a.Hkv);
+        ld_bt = a.block_tables + ((int64_t)r * a.B + b) * a.max_blocks;
+    };
+    ld_unit();
 
     // ---- producer: issue the copies of chunk cc into its ring stage
     auto issue = [&](int64_t cc) {
         if (cc < c1) {
-            while (unit_start[u_load + 1] <= cc) ++u_load;
-            const int r = (int)(u_load % a.N);
-            const int64_t bk = u_load / a.N;
-            const int b = (int)(bk / a.Hkv), kvh = (int)(bk % a.Hkv);
-            const int64_t p0 = (cc - unit_start[u_load]) * kChunk;
-            const int32_t blk = a.block_tables[((int64_t)r * a.B + b) * a.max_blocks + p0 / a.bs];
+            if (cc >= ld_end) {
+                while (unit_start[u_load + 1] <= cc) ++u_load;
+                ld_start = unit_start[u_load];
+                ld_end = unit_start[u_load + 1];
+                ld_unit();
+            }
+            const int p0 = (int)(cc - ld_start) * kChunk;
+            const int32_t blk = ld_bt[p0 / a.bs];
             if (blk >= 0 && blk < a.num_blocks) {
-                const int64_t row0 = ((int64_t)blk * a.Hkv + kvh) * a.bs + p0 % a.bs;
+                const int64_t row0 = ((int64_t)blk * a.Hkv + ld_kvh) * a.bs + p0 % a.bs;
                 const uint8_t* ks = reinterpret_cast<const uint8_t*>(kp + row0 * D);
                 const uint8_t* vs = reinterpret_cast<const uint8_t*>(vp + row0 * D);
                 const uint32_t st = wsm_u32 + (uint32_t)((cc - c0) % NST) * C::kStageBytes;
@@ -139,6 +154,10 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
     int64_t boundA = 0, boundB = 0;
     int64_t cur_group = -1, cur_bk = -1, cur_unit = -1;
     int cur_b = 0, cur_kvh = 0, cur_r = 0;
+    int64_t cu_start = 0, cu_end = -1, cu_bk = 0;
+    int cu_r = 0;
+    const int32_t* cu_bt = nullptr;
+    int fullvis = 0;  // chunks below this local position are visible to every row
     const float sl2 = a.softmax_scale * 1.4426950408889634f;  // log2(e)
 
     auto reset_state = [&]() {
@@ -248,10 +267,17 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
         cp_async_wait<NST - 1>();
         __syncwarp();
 
-        while (unit_start[u + 1] <= c) ++u;
-        const int r = (int)(u % a.N);
-        const int64_t bk = u / a.N;
-        const int b = (int)(bk / a.Hkv), kvh = (int)(bk % a.Hkv);
+        if (c >= cu_end) {
+            while (unit_start[u + 1] <= c) ++u;
+            cu_start = unit_start[u];
+            cu_end = unit_start[u + 1];
+            cu_r = (int)(u % a.N);
+            cu_bk = u / a.N;
+            cu_bt = a.block_tables + ((int64_t)cu_r * a.B + (int)(cu_bk / a.Hkv)) * a.max_blocks;
+        }
+        const int r = cu_r;
+        const int64_t bk = cu_bk;
+        const int b = (int)(bk / a.Hkv), kvh = (int)(bk - (int64_t)b * a.Hkv);
         const int64_t group = a.partial_mode ? u : bk;
         if (group != cur_group) {
             if (cur_group >= 0) flush(cur_group);
@@ -283,9 +309,11 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
             cur_unit = u;
             boundA = rowA < a.rows ? local_len(L - a.Tq + rowA / a.G + 1, r, a.N, a.I) : 0;
             boundB = rowB < a.rows ? local_len(L - a.Tq + rowB / a.G + 1, r, a.N, a.I) : 0;
+            // every row sees at least the first len(L - Tq + 1) local positions
+            fullvis = (int)local_len(L - a.Tq + 1, r, a.N, a.I);
         }
-        const int64_t p0 = (c - unit_start[u]) * kChunk;
-        const int32_t blk = a.block_tables[((int64_t)r * a.B + b) * a.max_blocks + p0 / a.bs];
+        const int p0 = (int)(c - cu_start) * kChunk;
+        const int32_t blk = cu_bt[p0 / a.bs];
         if (blk < 0 || blk >= a.num_blocks) {
             if (lane == 0) raise_err(err, DCP_DEV_ERR_BLOCK_ID);
             __syncwarp();
@@ -307,15 +335,21 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
                 mma_bf16(s[1], qf[ks], k2, k3);
             }
         }
-        // scale to base 2, mask, online softmax
+        // scale to base 2, mask (only a chunk some row cannot fully see), online
+        // softmax.  Rows past a.rows are padding: their values are never written.
         float mxA = -INFINITY, mxB = -INFINITY;
+        const bool all_visible = (p0 + kChunk <= fullvis);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const int64_t tok = p0 + nt * 8 + 2 * t4;
-            s[nt][0] = (tok < boundA) ? s[nt][0] * sl2 : -INFINITY;
-            s[nt][1] = (tok + 1 < boundA) ? s[nt][1] * sl2 : -INFINITY;
-            s[nt][2] = (tok < boundB) ? s[nt][2] * sl2 : -INFINITY;
-            s[nt][3] = (tok + 1 < boundB) ? s[nt][3] * sl2 : -INFINITY;
+            if (all_visible) {
+                s[nt][0] *= sl2; s[nt][1] *= sl2; s[nt][2] *= sl2; s[nt][3] *= sl2;
+            } else {
+                const int64_t tok = p0 + nt * 8 + 2 * t4;
+                s[nt][0] = (tok < boundA) ? s[nt][0] * sl2 : -INFINITY;
+                s[nt][1] = (tok + 1 < boundA) ? s[nt][1] * sl2 : -INFINITY;
+                s[nt][2] = (tok < boundB) ? s[nt][2] * sl2 : -INFINITY;
+                s[nt][3] = (tok + 1 < boundB) ? s[nt][3] * sl2 : -INFINITY;
+            }
             mxA = fmaxf(mxA, fmaxf(s[nt][0], s[nt][1]));
             mxB = fmaxf(mxB, fmaxf(s[nt][2], s[nt][3]));
         }
@@ -325,25 +359,28 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
         mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
         const float mnA = fmaxf(mA, mxA), mnB = fmaxf(mB, mxB);
         const float useA = (mnA == -INFINITY) ? 0.f : mnA, useB = (mnB == -INFINITY) ? 0.f : mnB;
-        const float corrA = exp2f(mA - useA), corrB = exp2f(mB - useB);
+        const bool changed = (mnA != mA) || (mnB != mB);
+        if (__any_sync(0xffffffffu, changed)) {
+            const float corrA = sm100::ex2_approx(mA - useA), corrB = sm100::ex2_approx(mB - useB);
+            lA *= corrA;
+            lB *= corrB;
+#pragma unroll
+            for (int j = 0; j < C::kNT; ++j) {
+                o[j][0] *= corrA; o[j][1] *= corrA;
+                o[j][2] *= corrB; o[j][3] *= corrB;
+            }
+        }
         mA = mnA;
         mB = mnB;
-        lA *= corrA;
-        lB *= corrB;
-#pragma unroll
-        for (int j = 0; j < C::kNT; ++j) {
-            o[j][0] *= corrA; o[j][1] *= corrA;
-            o[j][2] *= corrB; o[j][3] *= corrB;
-        }
         uint32_t pf[4];
         {
             float p[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                p[nt][0] = exp2f(s[nt][0] - useA);
-                p[nt][1] = exp2f(s[nt][1] - useA);
-                p[nt][2] = exp2f(s[nt][2] - useB);
-                p[nt][3] = exp2f(s[nt][3] - useB);
+                p[nt][0] = sm100::ex2_approx(s[nt][0] - useA);
+                p[nt][1] = sm100::ex2_approx(s[nt][1] - useA);
+                p[nt][2] = sm100::ex2_approx(s[nt][2] - useB);
+                p[nt][3] = sm100::ex2_approx(s[nt][3] - useB);
                 lA += p[nt][0] + p[nt][1];
                 lB += p[nt][2] + p[nt][3];
             }

@@ -42,7 +42,8 @@ __device__ int64_t block_inclusive_scan(int64_t v, int64_t* warp_tot) {
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     __shared__ int64_t warp_tot[32];
     __shared__ int64_t carry;
-    __shared__ int empty_flag[kPlanThreads];
+    __shared__ int empty_list[kPlanThreads];
+    __shared__ int n_empty;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
     int64_t* unit_start = reinterpret_cast<int64_t*>(a.ws + a.lay.off_units);
     int32_t* seg_base = reinterpret_cast<int32_t*>(a.ws + a.lay.off_seg_base);
@@ -111,15 +112,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     }
     if (tid == 0) seg_base[a.G] = (int32_t)carry;
 
-    // 3. groups that own no chunk: zeros and -inf
+    // 3. groups that own no chunk (rare): zeros and -inf.  Each thread checks
+    // its groups and appends the empty ones to a shared list.
     const int G = a.Hq / a.Hkv;
     for (int64_t base = 0; base < a.G; base += kPlanThreads) {
-        const int64_t g = base + tid;
-        empty_flag[tid] = (g < a.G) && unit_start[g * per_group] == unit_start[(g + 1) * per_group];
+        if (tid == 0) n_empty = 0;
         __syncthreads();
-        for (int k = 0; k < kPlanThreads && base + k < a.G; ++k) {
-            if (!empty_flag[k]) continue;
-            const int64_t gg = base + k;
+        const int64_t g = base + tid;
+        if (g < a.G && unit_start[g * per_group] == unit_start[(g + 1) * per_group])
+            empty_list[atomicAdd(&n_empty, 1)] = (int)tid;
+        __syncthreads();
+        for (int k = 0; k < n_empty; ++k) {
+            const int64_t gg = base + empty_list[k];
             int b, kvh, r = 0;
             if (a.partial_mode) {
                 r = (int)(gg % a.N);
