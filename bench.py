@@ -43,6 +43,32 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+# DRAM bytes per cached KV token of the attention kernel, from one ncu capture
+# each (dram__bytes_read.sum + dram__bytes_write.sum of one launch divided by
+# the launch's cached tokens; summaries and commands under profiles/).  Valid
+# only for the kernel source they were taken on: a changed source gives null.
+MEASURED_TRAFFIC = {
+    ("mla_tcgen05", "fp8"): ("attn_mla_tc.cu", "1c9047de99b63eb1de27eae0dc7925dad6aea2379a52ccb2eebb39034ac138cb",
+                             (219.003392e6 + 3.723776e6) / 376734),
+    ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "1c9047de99b63eb1de27eae0dc7925dad6aea2379a52ccb2eebb39034ac138cb",
+                              (304.139776e6 + 4.788736e6) / 262144),
+    ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "472cd388b3017692f89db1389a40a40652791550ac6d32b3e8a2fb95358a06ae",
+                          (268.720128e6 + 3.707392e6) / 65536),
+}
+
+
+def measured_traffic(kernel, kv_dtype, tokens):
+    import hashlib
+    entry = MEASURED_TRAFFIC.get((kernel, kv_dtype))
+    if entry is None:
+        return None
+    fname, sha, per_token = entry
+    path = os.path.join(ROOT, "context_decode_attention_gb300", "csrc", fname)
+    if not os.path.exists(path) or hashlib.sha256(open(path, "rb").read()).hexdigest() != sha:
+        return None
+    return per_token * tokens
+
+
 def algorithmic(wl):
     """Algorithmic bytes and FLOPs of one attention launch (every KV byte read once)."""
     c = wl.cfg
@@ -59,7 +85,7 @@ def algorithmic(wl):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms (best effort)."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms (best effort)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -71,7 +97,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
@@ -214,7 +240,7 @@ def workload_config(c, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="dcp", choices=["dcp", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -335,7 +361,9 @@ def main():
     else:
         roof = {"bound": "hbm", "achieved": alg["bytes"] / t_attn / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(kernel, cfg["kv_dtype"], int(wl.seq_lens.sum()))
+    roof["traffic_note"] = "ncu DRAM bytes per cached token of one capture (profiles/), scaled to this launch's tokens"
+    roof["algorithmic_bytes"] = alg["bytes"]
     roof["peak_source"] = peaks["source"] + " (MEASURED_PEAKS.json, burst)"
     roof["kernel"] = kernel
     roof["roofline_ms"] = 1e3 * max(t_mem, t_tc)
