@@ -94,7 +94,8 @@ bool layout_for(const dcp_params& p, int32_t B, WsLayout* out, Kernel* kout, int
     const int64_t U = (int64_t)B * p.Hkv * p.N;
     const int64_t w = k == Kernel::kNone ? 0 : kernel_workers(k, sms, p);
     const int64_t rows = (int64_t)p.Tq * (p.Hq / p.Hkv);
-    *out = ws_layout(U, U, w + U, rows, p.Dv);
+    const size_t qprep = (k == Kernel::kMlaTc && p.kv_dtype == DCP_FP8_E4M3) ? mla_f8_qprep_bytes(B, p.Tq) : 0;
+    *out = ws_layout(U, U, w + U, rows, p.Dv, qprep);
     if (kout) *kout = k;
     if (W) *W = w;
     return true;
@@ -154,7 +155,7 @@ int run_attention(const dcp_params* params, int32_t B, const void* q, const void
         count_launches(1);
     } else if (kern == Kernel::kMlaTc) {
         e = launch_attn_mla_tc(a, p.kv_dtype, stream);
-        count_launches(1);
+        count_launches(p.kv_dtype == DCP_FP8_E4M3 ? 2 : 1);  // fp8: query preparation + attention
         if (e == cudaSuccess && a.Gn > 0) {
             e = launch_segment_merge(a, stream);
             count_launches(1);

@@ -42,6 +42,7 @@ __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { r
 //   counters      uint32[G]      arrivals per group (fused merge)
 //   part_o        fp32[seg_max][rows][Dv]
 //   part_lse      fp32[seg_max][rows]
+//   qprep         kernel-specific staging of the query (fp8 MLA kernel), else empty
 // ---------------------------------------------------------------------------
 struct WsHeader {
     uint32_t err;
@@ -50,12 +51,13 @@ struct WsHeader {
 };
 
 struct WsLayout {
-    size_t off_units, off_seg_base, off_counters, off_part_o, off_part_lse, total;
+    size_t off_units, off_seg_base, off_counters, off_part_o, off_part_lse, off_qprep, total;
 };
 
 __host__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-__host__ inline WsLayout ws_layout(int64_t U, int64_t G, int64_t seg_max, int64_t rows, int64_t Dv) {
+__host__ inline WsLayout ws_layout(int64_t U, int64_t G, int64_t seg_max, int64_t rows, int64_t Dv,
+                                   size_t qprep_bytes = 0) {
     WsLayout l;
     size_t o = 256;
     l.off_units = o; o = align256(o + sizeof(int64_t) * (size_t)(U + 1));
@@ -63,6 +65,7 @@ __host__ inline WsLayout ws_layout(int64_t U, int64_t G, int64_t seg_max, int64_
     l.off_counters = o; o = align256(o + sizeof(uint32_t) * (size_t)(G + 1));
     l.off_part_o = o; o = align256(o + sizeof(float) * (size_t)seg_max * rows * Dv);
     l.off_part_lse = o; o = align256(o + sizeof(float) * (size_t)seg_max * rows);
+    l.off_qprep = o; o = align256(o + qprep_bytes);
     l.total = o;
     return l;
 }
@@ -150,6 +153,11 @@ cudaError_t launch_attn_gqa_mma(const AttnArgs& a, cudaStream_t s);
 bool mla_tc_supported(const dcp_params& p);
 int64_t mla_tc_workers(int num_sms, int Tq);
 cudaError_t launch_attn_mla_tc(const AttnArgs& a, int kv_dtype, cudaStream_t s);
+// the fp8-cache form (kind::f8f6f4, two-term query and probabilities): a query
+// preparation kernel, then the attention kernel; the prepared query lives in
+// the workspace's qprep region (mla_f8_qprep_bytes).
+size_t mla_f8_qprep_bytes(int64_t B, int Tq);
+cudaError_t launch_attn_mla_f8(const AttnArgs& a, cudaStream_t s);
 
 // standalone merge for dcp_lse_merge
 cudaError_t launch_lse_merge(int N, int64_t rows, int Dv, const float* o_parts, const float* lse_parts,
