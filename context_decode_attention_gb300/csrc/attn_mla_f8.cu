@@ -31,8 +31,8 @@
 // S = Q K^T.  A tile is up to two 64-token chunks.
 //
 // Warp roles (per CTA):
-//   warps 0-2  TMA producers: ring item k is issued by warp k % 3; warp 0
-//              also loads each segment's hi/lo query
+//   warps 0-2  TMA producers: TMA box b (two per ring item) is issued by
+//              warp b % 3; warp 0 also loads each segment's hi/lo query
 //   warp 3     TMEM owner and MMA issuer (one lane)
 //   warps 4-7  softmax / O correction / segment epilogue, thread = head
 // Ring items per tile: K sub-tiles 0-4 (columns 128 s .. 128 s + 127; the
@@ -280,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < kProd) {
         // ------------------------------------------------------------ TMA producers
         // Items are numbered in consumption order; item k goes to ring slot
-        // k % kRing and is issued by producer warp k % kProd.  Block ids are
-        // read once per tile, one tile ahead of their use.
+        // k % kRing.  Block ids are read once per tile, one tile ahead of
+        // their use.
         if (lane == 0) {
             const int me = warp;
             Ring ring;
@@ -307,25 +307,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t p = (x.t.chunk + k) * kChunk;
                 return (int)((int64_t)blk * a.bs + p % a.bs);
             };
-            int64_t item = 0;
+            // TMA boxes are dealt to the producer warps in turn (box b to warp
+            // b % kProd), so the two boxes of an item go out from two warps at
+            // once; the warp with an item's first box posts its byte count.
+            int64_t box = 0;
             auto pad_item = [&]() {
-                if ((int)(item % kProd) == me) {
+                if ((int)(box % kProd) == me) {
                     if (!mbar_wait_sleep(&sh.empty[ring.slot], ring.phase ^ 1u)) { alive = false; return; }
                     mbar_arrive(&sh.full[ring.slot]);
                 }
-                ++item;
+                ++box;
                 ring.advance();
             };
             auto load_sub = [&](const Ahead& x, int col) {
-                if ((int)(item % kProd) == me) {
-                    if (!mbar_wait_sleep(&sh.empty[ring.slot], ring.phase ^ 1u)) { alive = false; return; }
-                    constexpr int box_bytes = kChunk * kSubCols;  // 8192, zeros past column 575 included
-                    mbar_arrive_expect_tx(&sh.full[ring.slot], (uint32_t)(box_bytes * x.t.n_ch));
-                    uint8_t* dst = sRing + ring.slot * kSubBytes;
-                    for (int k = 0; k < x.t.n_ch; ++k)
-                        tma_load_2d(dst + k * box_bytes, &tmap_kv, col, row_of(x, k), &sh.full[ring.slot]);
+                constexpr int box_bytes = kChunk * kSubCols;  // 8192, zeros past column 575 included
+                uint8_t* dst = sRing + ring.slot * kSubBytes;
+                bool waited = false;
+                for (int k = 0; k < x.t.n_ch; ++k, ++box) {
+                    if ((int)(box % kProd) != me) continue;
+                    if (!waited) {
+                        if (!mbar_wait_sleep(&sh.empty[ring.slot], ring.phase ^ 1u)) { alive = false; return; }
+                        waited = true;
+                    }
+                    if (k == 0) mbar_arrive_expect_tx(&sh.full[ring.slot], (uint32_t)(box_bytes * x.t.n_ch));
+                    tma_load_2d(dst + k * box_bytes, &tmap_kv, col, row_of(x, k), &sh.full[ring.slot]);
                 }
-                ++item;
                 ring.advance();
             };
             Ahead cur_t, nxt, prev;
@@ -346,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 9; ++j) tma_load_2d(smem + j * kSubBytes, &tmap_q, 128 * j, row0, sh.q_full);
                 }
                 if (cur_t.valid) {
-                    if ((int)(item % kProd) == me) {
+                    if ((int)(box % kProd) == me) {
                         TileMsg m;
                         m.n_ch = cur_t.t.n_ch;
                         m.first = cur_t.t.first;
@@ -397,23 +403,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int sb = ti & 1;
                     const uint32_t d = tm + 256 + 128 * sb;
                     const uint32_t idesc_qk = idesc_e4m3(128, 64 * t.n_ch, 0, 0);
+                    // K sub-tile s against query hi and lo: sub-tiles 0-3 four 32-column
+                    // k-steps each; the tail (columns 512-575) two, its hi in bytes 0-63
+                    // and lo in bytes 64-127 of the tail query sub-tile
+#pragma unroll 1
                     for (int s = 0; s < kKItems; ++s) {
                         if (s > 0 && !mbar_wait_sleep(&sh.full[ring.slot], ring.phase)) { alive = false; break; }
                         tc_fence_after();
                         const uint64_t kd = dk + ring.slot * kSubDesc;
-                        if (s < kKItems - 1) {
-                            const uint64_t ah = dq + ((kOffQHi + s * kSubBytes) >> 4);
-                            const uint64_t al = dq + ((kOffQLo + s * kSubBytes) >> 4);
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) mma_f8_ss(d, ah + 2 * kk, kd + 2 * kk, idesc_qk, (s | kk) != 0);
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) mma_f8_ss(d, al + 2 * kk, kd + 2 * kk, idesc_qk, 1u);
-                        } else {
-                            // columns 512-575: bytes 0-63 of the K rows against hi (bytes 0-63)
-                            // and lo (bytes 64-127) of the tail query sub-tile
-                            const uint64_t at = dq + (kOffQTail >> 4);
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) mma_f8_ss(d, at + 2 * kk, kd + 2 * (kk & 1), idesc_qk, 1u);
+                        const bool tail = s == kKItems - 1;
+                        const uint64_t ah = dq + (tail ? (kOffQTail >> 4) : ((kOffQHi + s * kSubBytes) >> 4));
+                        const uint64_t al = dq + (tail ? ((kOffQTail + 64) >> 4) : ((kOffQLo + s * kSubBytes) >> 4));
+                        const int nk = tail ? 2 : 4;
+#pragma unroll 1
+                        for (int kk = 0; kk < nk; ++kk) {
+                            mma_f8_ss(d, ah + 2 * kk, kd + 2 * kk, idesc_qk, (s | kk) != 0);
+                            mma_f8_ss(d, al + 2 * kk, kd + 2 * kk, idesc_qk, 1u);
                         }
                         mma_commit(&sh.empty[ring.slot]);
                         ring.advance();
