@@ -19,8 +19,9 @@
 // K and V stream through a ring of [tile x 64-column] sub-tiles.
 //
 // Warp roles (per CTA):
-//   warps 0-2     TMA producers: ring item k is issued by warp k % 3 (one TMA
-//                 instruction occupies its issuing warp for ~440 cycles)
+//   warps 0-2     TMA producers: TMA box b (two per ring item) is issued by
+//                 warp b % 3 (one TMA instruction occupies its issuing warp
+//                 for ~440 cycles)
 //   warp 3        TMEM owner and MMA issuer (one lane)
 //   warps 4-7     softmax / O correction / segment epilogue; thread = head
 // TMEM: O half [0, 256), S double buffer [256, 384) and [384, 512); P is
@@ -61,8 +62,17 @@ constexpr int kOffRing = kQBytes;
 constexpr int kOffBar = kOffRing + kRing * kSubBytes;
 constexpr int kNumBars = 2 * kRing + 7;
 constexpr int kOffUnits = kOffBar + kNumBars * 8 + 16;
-constexpr int kSmem = kOffUnits + kUnitCache * 8 + 1024;  // + alignment slack
+constexpr int kTileRing = 8;  // tile descriptors handed from the producers to the MMA issuer
+constexpr int kOffTiles = kOffUnits + kUnitCache * 8;
+constexpr int kSmem = kOffTiles + kTileRing * 16 + 1024;  // + alignment slack
 static_assert(kSmem <= 232448, "shared memory");
+
+// One tile as the producers saw it, for the MMA issuer (which then needs no
+// cursor of its own): written before the arrive that publishes the tile's
+// first K sub-tile, read after the wait on it.
+struct TileMsg {
+    int32_t n_ch, first, last, has_next;
+};
 
 struct Bars {
     uint64_t *full, *empty, *q_full, *q_empty, *s_full, *p_full, *o_done;
@@ -96,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sQ = smem + kOffQ;
     uint8_t* sRing = smem + kOffRing;
     int64_t* us_s = reinterpret_cast<int64_t*>(smem + kOffUnits);
+    TileMsg* tmsg = reinterpret_cast<TileMsg*>(smem + kOffTiles);
     const Bars sh = carve(smem);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -144,9 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < kProd) {
         // ------------------------------------------------------------ TMA producers
         // The ring items (K sub-tiles of tile t, then V sub-tiles of tile t-1)
-        // are numbered in consumption order; item k goes to ring slot k % kRing
-        // and is issued by producer warp k % kProd.  Block ids are read once per
-        // tile, one tile ahead of their use.
+        // are numbered in consumption order; item k goes to ring slot
+        // k % kRing.  Block ids are read once per tile, one tile ahead of
+        // their use.
         if (lane == 0) {
             const int me = warp;
             Ring ring;
@@ -172,26 +183,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t p = (x.t.chunk + k) * kChunk;
                 return (int)((int64_t)blk * a.bs + p % a.bs);
             };
-            int64_t item = 0;  // global item index in consumption order
+            // TMA boxes are dealt to the producer warps in turn (box b to warp
+            // b % kProd), so the two boxes of an item go out from two warps at
+            // once; the warp with an item's first box posts its byte count.
+            int64_t box = 0;
             // a no-op item: keeps the ring aligned (the MMA warp just releases it)
             auto pad_item = [&]() {
-                if ((int)(item % kProd) == me) {
-                    if (!mbar_wait(&sh.empty[ring.slot], ring.phase ^ 1u)) { alive = false; return; }
+                if ((int)(box % kProd) == me) {
+                    if (!mbar_wait_sleep(&sh.empty[ring.slot], ring.phase ^ 1u)) { alive = false; return; }
                     mbar_arrive(&sh.full[ring.slot]);
                 }
-                ++item;
+                ++box;
                 ring.advance();
             };
             auto load_sub = [&](const Ahead& x, int col) {
-                if ((int)(item % kProd) == me) {
-                    if (!mbar_wait(&sh.empty[ring.slot], ring.phase ^ 1u)) { alive = false; return; }
-                    constexpr int box_bytes = kChunk * 128;
-                    mbar_arrive_expect_tx(&sh.full[ring.slot], (uint32_t)(box_bytes * x.t.n_ch));
-                    uint8_t* dst = sRing + ring.slot * kSubBytes;
-                    for (int k = 0; k < x.t.n_ch; ++k)
-                        tma_load_2d(dst + k * box_bytes, &tmap_kv, col, row_of(x, k), &sh.full[ring.slot]);
+                constexpr int box_bytes = kChunk * 128;
+                uint8_t* dst = sRing + ring.slot * kSubBytes;
+                bool waited = false;
+                for (int k = 0; k < x.t.n_ch; ++k, ++box) {
+                    if ((int)(box % kProd) != me) continue;
+                    if (!waited) {
+                        if (!mbar_wait_sleep(&sh.empty[ring.slot], ring.phase ^ 1u)) { alive = false; return; }
+                        waited = true;
+                    }
+                    if (k == 0) mbar_arrive_expect_tx(&sh.full[ring.slot], (uint32_t)(box_bytes * x.t.n_ch));
+                    tma_load_2d(dst + k * box_bytes, &tmap_kv, col, row_of(x, k), &sh.full[ring.slot]);
                 }
-                ++item;
                 ring.advance();
             };
             Ahead cur_t, nxt, prev;
@@ -204,13 +221,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const Tile& t = cur_t.t;
                     if (t.first && me == 0) {
                         if (ti > 0) {
-                            if (!mbar_wait(sh.q_empty, qe_phase)) { alive = false; break; }
+                            if (!mbar_wait_sleep(sh.q_empty, qe_phase)) { alive = false; break; }
                             qe_phase ^= 1u;
                         }
                         const int b = (int)((uint32_t)t.u / (uint32_t)a.N);
                         const int row0 = (int)(((int64_t)b * a.Tq + tq) * kHeads);
                         mbar_arrive_expect_tx(sh.q_full, kQBytes);
                         for (int j = 0; j < kKSub; ++j) tma_load_2d(sQ + j * 16384, &tmap_q, 64 * j, row0, sh.q_full);
+                    }
+                    if ((int)(box % kProd) == me) {
+                        TileMsg m;
+                        m.n_ch = t.n_ch;
+                        m.first = t.first;
+                        m.last = t.last;
+                        m.has_next = nxt.valid;
+                        tmsg[ti % kTileRing] = m;
                     }
                     for (int s2 = 0; s2 < kKSub && alive; ++s2) load_sub(cur_t, 64 * s2);
                 }
@@ -234,28 +259,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             ring.n = kRing;
             uint32_t qf_phase = 0, pf_phase[2] = {0u, 0u};
             bool alive = true;
-            Tile prev{}, t{};
+            TileMsg prev{}, t{};
             int ti = 0;
+            // descriptors (start address in 16-byte units in the low bits): Q
+            // sub-tile s at dq + 1024 s, ring slot i at dk + 1024 i, +2 per
+            // 32-byte k-step; V MN-major with its 64-column blocks one slot apart
+            const uint64_t dq = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSW128);
+            const uint64_t dk = smem_desc(smem_u32(sRing), 16, 1024, kLayoutSW128);
+            const uint64_t dv = smem_desc(smem_u32(sRing + 1 * kSubBytes), kSubBytes, 1024, kLayoutSW128);
+            constexpr uint32_t kSubDesc = kSubBytes >> 4;
             const uint32_t idesc_pv = idesc_f16(1, 128, 256, 0, 1);
+            bool more = true;  // every worker owns at least one chunk
             for (;;) {
-                const bool more = cur.next(t);
                 if (more) {
+                    if (!mbar_wait_sleep(&sh.full[ring.slot], ring.phase)) { alive = false; break; }
+                    t = tmsg[ti % kTileRing];
                     if (t.first) {
-                        if (!mbar_wait(sh.q_full, qf_phase)) { alive = false; break; }
+                        if (!mbar_wait_sleep(sh.q_full, qf_phase)) { alive = false; break; }
                         qf_phase ^= 1u;
                     }
                     const int sb = ti & 1;
                     const uint32_t d = tm + 256 + 128 * sb;
                     const uint32_t idesc_qk = idesc_f16(1, 128, 64 * t.n_ch, 0, 0);
+#pragma unroll 1
                     for (int s = 0; s < kKSub; ++s) {
-                        if (!mbar_wait(&sh.full[ring.slot], ring.phase)) { alive = false; break; }
+                        if (s > 0 && !mbar_wait_sleep(&sh.full[ring.slot], ring.phase)) { alive = false; break; }
                         tc_fence_after();
-                        const uint32_t kb = smem_u32(sRing + ring.slot * kSubBytes);
-                        const uint32_t qb = smem_u32(sQ + s * 16384);
+                        const uint64_t kd = dk + ring.slot * kSubDesc, qd = dq + s * kSubDesc;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(d, smem_desc(qb + kk * 32, 16, 1024, kLayoutSW128),
-                                   smem_desc(kb + kk * 32, 16, 1024, kLayoutSW128), idesc_qk, (s | kk) != 0);
+                        for (int kk = 0; kk < 4; ++kk) mma_ss(d, qd + 2 * kk, kd + 2 * kk, idesc_qk, (s | kk) != 0);
                         mma_commit(&sh.empty[ring.slot]);
                         ring.advance();
                     }
@@ -266,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // consume the padding items that realign the ring
                 const uint32_t target = (ti > 0) ? 1u : 0u;
                 while (ring.slot != target) {
-                    if (!mbar_wait(&sh.full[ring.slot], ring.phase)) { alive = false; break; }
+                    if (!mbar_wait_sleep(&sh.full[ring.slot], ring.phase)) { alive = false; break; }
                     mbar_arrive(&sh.empty[ring.slot]);
                     ring.advance();
                 }
@@ -274,17 +306,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ti > 0) {
                     // O[:, half] += P V with V's four 64-column blocks in slots 1..4
                     const int sb = (ti - 1) & 1;
-                    if (!mbar_wait(&sh.p_full[sb], pf_phase[sb])) { alive = false; break; }
+                    if (!mbar_wait_sleep(&sh.p_full[sb], pf_phase[sb])) { alive = false; break; }
                     pf_phase[sb] ^= 1u;
                     for (int j = 0; j < kVSub; ++j)
-                        if (!mbar_wait(&sh.full[1 + j], ring.phase)) { alive = false; break; }
+                        if (!mbar_wait_sleep(&sh.full[1 + j], ring.phase)) { alive = false; break; }
                     if (!alive) break;
                     tc_fence_after();
                     const uint32_t pa = tm + 256 + 128 * sb;
-                    const uint32_t vb = smem_u32(sRing + 1 * kSubBytes);
+#pragma unroll 1
                     for (int kk = 0; kk < 4 * prev.n_ch; ++kk)
-                        mma_ts(tm_o, pa + 8 * kk, smem_desc(vb + kk * 2048, kSubBytes, 1024, kLayoutSW128), idesc_pv,
-                               !(prev.first && kk == 0));
+                        mma_ts(tm_o, pa + 8 * kk, dv + 128 * kk, idesc_pv, !(prev.first && kk == 0));
                     for (int j = 0; j < kVSub; ++j) {
                         mma_commit(&sh.empty[ring.slot]);
                         ring.advance();
@@ -292,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(sh.o_done);
                 }
                 if (!more) break;
+                more = t.has_next;
                 prev = t;
                 ++ti;
             }
@@ -361,33 +393,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&sh.s_full[sb], sf_phase[sb])) { alive = false; break; }
             sf_phase[sb] ^= 1u;
             tc_fence_after();
-            const int64_t p0 = t.chunk * kChunk;
             const uint32_t sbase = tm + 256 + 128 * sb + lane_off;
             const int ncols = 64 * t.n_ch;
             // columns [0, lim) are visible to this query token
-            const int64_t lim64 = bound - p0;
+            const int64_t lim64 = bound - t.chunk * kChunk;
             const int lim = lim64 <= 0 ? 0 : (lim64 >= ncols ? ncols : (int)lim64);
-            float sv[128];
-            uint32_t rr[32];
-#pragma unroll
-            for (int cch = 0; cch < 4; ++cch) {
-                if (cch * 32 < ncols) {
-                    tmem_ld32(sbase + 32 * cch, rr);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) sv[32 * cch + k] = __uint_as_float(rr[k]);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) sv[32 * cch + k] = 0.f;
-                }
-            }
+            // pass 1: the tile's row maximum, 32 columns at a time (small loop
+            // bodies: these warps are bound by instruction fetch, not arithmetic)
             float mraw = -INFINITY;
-            if (lim == 128) {
+            {
+                uint32_t rr[32];
+#pragma unroll 1
+                for (int c = 0; c < ncols / 32; ++c) {
+                    tmem_ld32(sbase + 32 * c, rr);
+                    tmem_wait_ld();
+                    const int lc = lim - 32 * c;
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int j = 0; j < 128; ++j) mraw = fmaxf(mraw, sv[j]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 128; ++j) mraw = (j < lim) ? fmaxf(mraw, sv[j]) : mraw;
+                    for (int k = 0; k < 32; ++k)
+                        m4[k & 3] = fmaxf(m4[k & 3], (k < lc) ? __uint_as_float(rr[k]) : -INFINITY);
+                    mraw = fmaxf(mraw, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                }
             }
             const float mx = (lim > 0) ? mraw * sl2 : -INFINITY;
             // lazy reference max
@@ -404,25 +430,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            // pass 2: 16 columns at a time; their bf16 pairs go to columns
+            // [8 q, 8 q + 8), which earlier steps have already read
             float lsum = 0.f;
-            uint32_t pk[32];
+#pragma unroll 1
+            for (int q = 0; q < ncols / 16; ++q) {
+                uint32_t r16[16], pk[8];
+                tmem_ld16(sbase + 16 * q, r16);
+                tmem_wait_ld();
+                const int lq = lim - 16 * q;
+                float ls2[2] = {0.f, 0.f};
 #pragma unroll
-            for (int cch = 0; cch < 2; ++cch) {
-                if (cch * 64 < ncols) {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int j = 64 * cch + 2 * k;
-                        float p_lo = ex2_approx(fmaf(sv[j], sl2, nmu));
-                        float p_hi = ex2_approx(fmaf(sv[j + 1], sl2, nmu));
-                        if (lim < 128) {
-                            p_lo = (j < lim) ? p_lo : 0.f;
-                            p_hi = (j + 1 < lim) ? p_hi : 0.f;
-                        }
-                        lsum += p_lo + p_hi;
-                        pk[k] = pack_bf16(p_lo, p_hi);
-                    }
-                    tmem_st32(tm + 256 + 128 * sb + lane_off + 32 * cch, pk);
+                for (int k = 0; k < 8; ++k) {
+                    const float s0 = (2 * k < lq) ? __uint_as_float(r16[2 * k]) : -INFINITY;
+                    const float s1 = (2 * k + 1 < lq) ? __uint_as_float(r16[2 * k + 1]) : -INFINITY;
+                    const float p0 = ex2_approx(fmaf(s0, sl2, nmu)), p1 = ex2_approx(fmaf(s1, sl2, nmu));
+                    ls2[0] += p0;
+                    ls2[1] += p1;
+                    pk[k] = pack_bf16(p0, p1);
                 }
+                lsum += ls2[0] + ls2[1];
+                tmem_st8(sbase + 8 * q, pk);
             }
             l = (corr == 0.f ? 0.f : l * corr) + lsum;
             // PV of the previous tile must be complete before O is touched
