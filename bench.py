@@ -48,10 +48,10 @@ def load_peaks():
 # the launch's cached tokens; summaries and commands under profiles/).  Valid
 # only for the kernel source they were taken on: a changed source gives null.
 MEASURED_TRAFFIC = {
-    ("mla_tcgen05", "fp8"): ("attn_mla_tc.cu", "1c9047de99b63eb1de27eae0dc7925dad6aea2379a52ccb2eebb39034ac138cb",
-                             (219.003392e6 + 3.723776e6) / 376734),
-    ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "1c9047de99b63eb1de27eae0dc7925dad6aea2379a52ccb2eebb39034ac138cb",
-                              (304.139776e6 + 4.788736e6) / 262144),
+    ("mla_tcgen05", "fp8"): ("attn_mla_f8.cu", "e7e37847eb59021a5e349c2a40323bd8c63601405a2118c97056fb79a3c50c38",
+                             (219.009024e6 + 4.173568e6) / 376734),
+    ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "6b7676725f33dc6503c889bff4fb6f14704e91ed09891ab0aba86be609714753",
+                              (304.090624e6 + 4.698112e6) / 262144),
     ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "472cd388b3017692f89db1389a40a40652791550ac6d32b3e8a2fb95358a06ae",
                           (268.720128e6 + 3.707392e6) / 65536),
 }
