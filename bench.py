@@ -372,7 +372,11 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if kernel in ("gqa_mma", "mla_tcgen05") else "f32",
+        # the operand type of the dominant kernel's products (accumulation is fp32 throughout):
+        # bf16 tensor-core MMAs, e4m3 (kind::f8f6f4, two-term query and P) on the fp8 cache,
+        # fp32 on the CUDA-core path
+        "dtype": ("e4m3" if cfg["kv_dtype"] == "fp8" else "bf16") if kernel == "mla_tcgen05"
+                 else ("bf16" if kernel == "gqa_mma" else "f32"),
         "data": "synthetic (seeded; stands in for the pages' agentic ~67K-median trace)",
         "config": workload_config(cfg, wl),
         "kv_read_tbps": alg["kv_bytes"] / t_attn / 1e12,
