@@ -237,6 +237,139 @@ def workload_config(c, wl):
     }
 
 
+TRANSFER_METRIC = "PD block-transfer listing: requests/s (per-rank non-empty blocks and fills, 1 GB300)"
+
+
+def run_transfer(args):
+    """Time the block-transfer listing (dcp_transfer_blocks) on the workload's
+    block tables: the blocks each rank moves under prefill-decode
+    disaggregation, their token counts and the batch's fill.  The inputs are a
+    few MB, so L2 is flushed (a 256 MB write) between timed launches and each
+    launch is timed alone with CUDA events."""
+    import torch
+    import context_decode_attention_gb300 as dcp
+    from context_decode_attention_gb300.harness import DeviceWorkload
+    import oracle
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    over = {"B": args.batch} if args.batch else {}
+    if args.context:
+        over["L"] = args.context
+    cfg = config(args.workload, **over)
+    wl = make_workload(cfg, seed=int(cfg["index"]) + 1000 * rank)
+    dw = DeviceWorkload(wl, device=dev, populate=False)
+    stream = dw.stream
+    N, B, M = (int(x) for x in dw.block_tables.shape)
+    bs = int(cfg["block_size"])
+    counts = torch.empty((N, B), dtype=torch.int32, device=dev)
+    blocks = torch.empty((N, B, M), dtype=torch.int32, device=dev)
+    fills = torch.empty((N, B, M), dtype=torch.int32, device=dev)
+    totals = torch.empty(2, dtype=torch.int64, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    peaks = load_peaks()
+
+    def launch():
+        dcp.dcp_transfer_blocks(dw.params, dw.seq_lens, dw.block_tables, dw.num_blocks, counts, blocks, fills,
+                                totals, workspace=dw.workspace, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            launch()
+    torch.cuda.synchronize()
+    if dw.error_bits() != 0:
+        raise SystemExit("device error bits set during warm-up")
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = dcp.dcp_launch_count()
+    with torch.cuda.stream(stream):
+        for k in range(K):
+            flush.fill_(k & 255)
+            ev[k][0].record(stream)
+            launch()
+            ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    launches = dcp.dcp_launch_count() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    if dw.error_bits() != 0:
+        raise SystemExit("device error bits set during the timed region")
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+
+    # algorithmic bytes of one launch: the lengths and the listed table
+    # entries read once; counts, blocks, fills and totals written once
+    ref = oracle.transfer_blocks(N, int(cfg["I"]), bs, wl.seq_lens, dw.block_tables_host, dw.num_blocks)
+    got = [t.cpu().numpy() for t in (counts, blocks, fills, totals)]
+    exact = all(np.array_equal(g, ref[k]) for g, k in zip(got, ("counts", "blocks", "fills", "totals")))
+    if not exact:
+        raise SystemExit("transfer listing differs from the oracle")
+    listed = int(ref["counts"].sum())
+    alg_bytes = 4 * B + 4 * listed + 4 * N * B + 2 * 4 * N * B * M + 16
+
+    e2e = None
+    if not args.no_e2e:
+        sl_h = dw.seq_lens.cpu().pin_memory()
+        bt_h = dw.block_tables.cpu().pin_memory()
+        outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (counts, blocks, fills, totals)]
+        h2d = sl_h.numel() * 4 + bt_h.numel() * 4
+        d2h = sum(t.numel() * t.element_size() for t in outs_h)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(K):
+                dw.seq_lens.copy_(sl_h, non_blocking=True)
+                dw.block_tables.copy_(bt_h, non_blocking=True)
+                launch()
+                for h, d in zip(outs_h, (counts, blocks, fills, totals)):
+                    h.copy_(d, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max([e0.elapsed_time(e1) / K], world)[0]
+        e2e = {"value": world * B / (e2e_ms / 1e3), "unit": "requests/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+
+    ms = reduce_max([ms], world)[0]
+    achieved = alg_bytes / (ms / 1e3) / 1e9
+    tot = ref["totals"]
+    line = {
+        "metric": TRANSFER_METRIC, "value": world * B / (ms / 1e3), "unit": "requests/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32", "data": "synthetic (seeded block tables of the workload)",
+        "config": dict(workload_config(cfg, wl), op="transfer-blocks", max_blocks=M,
+                       l2="flushed (256 MB write) before every timed launch"),
+        "blocks_listed": listed, "slots_moved": int(tot[0]), "tokens_moved": int(tot[1]),
+        "transfer_fill": float(tot[1]) / max(1, int(tot[0])),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg_bytes,
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json, burst)",
+                     "kernel": "transfer_blocks_kernel"},
+        "gpu_launches": int(launches), "clocks": clk, "e2e": e2e, "parity": "bit-exact vs oracle",
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 2.0 or reps < 3:
+            oracle.transfer_blocks(N, int(cfg["I"]), bs, wl.seq_lens, dw.block_tables_host, dw.num_blocks)
+            reps += 1
+        dt = (time.perf_counter() - t0) / reps
+        line["cpu_baseline"] = {"value": B / dt, "unit": "requests/s", "cores": 1, "kind": "oracle",
+                                "sample": f"the whole batch, {reps} repetitions, token-by-token enumeration in C"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -248,10 +381,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling a smaller case)")
     ap.add_argument("--context", type=int, default=0, help="override to one fixed context length")
+    ap.add_argument("--op", default="decode", choices=["decode", "transfer-blocks"],
+                    help="decode: the decode step (default); transfer-blocks: the PD block-transfer listing")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "transfer-blocks":
+        return run_transfer(args)
 
     import torch
     import context_decode_attention_gb300 as dcp

@@ -6,7 +6,7 @@ build.py).  PyTorch supplies device memory and streams.  Nothing here falls
 back to the CPU: if the library is missing or cannot load, every call raises.
 
 Functions carry the C ABI's names (include/dcp.h):
-  dcp_workspace_size, dcp_workspace_init, dcp_get_error, dcp_slot_mapping,
+  dcp_workspace_size, dcp_workspace_init, dcp_get_error, dcp_slot_mapping, dcp_transfer_blocks,
   dcp_partial_attention, dcp_lse_merge, dcp_decode_attention
 """
 
@@ -20,7 +20,7 @@ from ._lib import (
 
 __all__ = [
     "DcpError", "DcpParams", "params_from_config", "lib", "lib_path",
-    "dcp_workspace_size", "dcp_workspace_init", "dcp_get_error", "dcp_slot_mapping",
+    "dcp_workspace_size", "dcp_workspace_init", "dcp_get_error", "dcp_slot_mapping", "dcp_transfer_blocks",
     "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention", "dcp_decode_attention_noalloc",
     "dcp_launch_count",
     "dcp_attention_kernel", "DCP_F32", "DCP_BF16", "DCP_FP8_E4M3", "DCP_LAYOUT_GQA", "DCP_LAYOUT_MLA",
@@ -102,6 +102,16 @@ def dcp_slot_mapping(params, seq_lens, tok_req=None, tok_pos=None, block_tables=
                                   _ptr(local_lens), _ptr(virt_blocks), _ptr(rank_blocks), _ptr(new_k),
                                   _ptr(new_v), _ptr(k_pool), _ptr(v_pool), _ptr(workspace),
                                   _nbytes(workspace), _stream(stream)), "dcp_slot_mapping")
+
+
+def dcp_transfer_blocks(params, seq_lens, block_tables, num_blocks, counts, blocks=None, fills=None,
+                        totals=None, workspace=None, stream=None):
+    """Per-rank non-empty blocks of each request with their token counts (and
+    the batch's slots / tokens moved in totals[2]); see include/dcp.h."""
+    _check(lib().dcp_transfer_blocks(ctypes.byref(params), int(seq_lens.numel()), _ptr(seq_lens),
+                                     _ptr(block_tables), int(block_tables.shape[-1]), int(num_blocks),
+                                     _ptr(counts), _ptr(blocks), _ptr(fills), _ptr(totals), _ptr(workspace),
+                                     _nbytes(workspace), _stream(stream)), "dcp_transfer_blocks")
 
 
 def dcp_partial_attention(params, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens,

@@ -49,6 +49,7 @@ int validate_params(const dcp_params* p) {
 }
 
 bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15) == 0; }
+bool aligned8(const void* ptr) { return ((uintptr_t)ptr & 7) == 0; }
 
 enum class Kernel { kNone, kGeneric, kGqaMma, kMlaTc };
 
@@ -254,6 +255,28 @@ int dcp_slot_mapping(const dcp_params* params, int32_t B, const int32_t* seq_len
     a.rank_blocks = rank_blocks; a.new_k = new_k; a.new_v = new_v; a.k_pool = k_pool; a.v_pool = v_pool;
     a.err = &reinterpret_cast<WsHeader*>(workspace)->err;
     return launch_slot_mapping(a, stream) == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
+int dcp_transfer_blocks(const dcp_params* params, int32_t B, const int32_t* seq_lens,
+                        const int32_t* block_tables, int32_t max_blocks, int64_t num_blocks, int32_t* counts,
+                        int32_t* blocks, int32_t* fills, int64_t* totals, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+    int rc = validate_params(params);
+    if (rc != DCP_OK) return rc;
+    const dcp_params& p = *params;
+    if (B < 0) return DCP_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < 256) return DCP_ERR_WORKSPACE;
+    if (B == 0) {
+        if (totals && cudaMemsetAsync(totals, 0, 2 * sizeof(int64_t), stream) != cudaSuccess) return DCP_ERR_CUDA;
+        return DCP_OK;
+    }
+    if (!seq_lens || !block_tables || !counts || max_blocks < 1 || num_blocks < 1) return DCP_ERR_INVALID_ARG;
+    if (!aligned8(totals)) return DCP_ERR_INVALID_ARG;
+    return launch_transfer_blocks(p.N, p.I, p.block_size, B, max_blocks, num_blocks, seq_lens, block_tables,
+                                  counts, blocks, fills, totals, &reinterpret_cast<WsHeader*>(workspace)->err,
+                                  stream) == cudaSuccess
+               ? DCP_OK
+               : DCP_ERR_CUDA;
 }
 
 int dcp_partial_attention(const dcp_params* params, int32_t B, const void* q, const void* k_pool,

@@ -159,6 +159,12 @@ cudaError_t launch_attn_mla_tc(const AttnArgs& a, int kv_dtype, cudaStream_t s);
 size_t mla_f8_qprep_bytes(int64_t B, int Tq);
 cudaError_t launch_attn_mla_f8(const AttnArgs& a, cudaStream_t s);
 
+// blocks moved under prefill-decode disaggregation (dcp_transfer_blocks)
+cudaError_t launch_transfer_blocks(int N, int I, int bs, int B, int max_blocks, int64_t num_blocks,
+                                   const int32_t* seq_lens, const int32_t* block_tables, int32_t* counts,
+                                   int32_t* blocks, int32_t* fills, int64_t* totals, uint32_t* err,
+                                   cudaStream_t s);
+
 // standalone merge for dcp_lse_merge
 cudaError_t launch_lse_merge(int N, int64_t rows, int Dv, const float* o_parts, const float* lse_parts,
                              void* out, int out_dtype, float* lse, cudaStream_t s);

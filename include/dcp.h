@@ -170,6 +170,35 @@ int dcp_slot_mapping(const dcp_params* params, int32_t B, const int32_t* seq_len
                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Blocks to move under prefill-decode disaggregation ("Breaking the
+ * Long-Sequence Inference Bottleneck ...", section 2, "Practical
+ * considerations for PD disaggregation"): KV moves between nodes in whole
+ * blocks, and a block that holds no token need not move.  For every rank r
+ * and request b (global lengths seq_lens[B], device int32), lists the physical
+ * blocks that hold at least one of the request's tokens, in block-table order,
+ * with their token counts.  A rank fills its blocks in local-position order,
+ * so these are the first ceil(local_len / block_size) table entries, all full
+ * but the last.
+ *   counts[N][B]              (required) listed blocks per rank and request
+ *   blocks[N][B][max_blocks]  (optional) their ids, -1 after the last
+ *   fills[N][B][max_blocks]   (optional) tokens in each block, 0 after the last
+ *   totals[2]                 (optional, 8-byte aligned, int64) the batch's
+ *                             block slots moved (sum of counts * block_size)
+ *                             and tokens moved; totals[1] / totals[0] is the
+ *                             fill of the transfer
+ * All outputs are device memory owned by the caller; block_tables as for
+ * dcp_slot_mapping.  Device checks: a listed table entry outside
+ * [0, num_blocks) -> DCP_DEV_ERR_BLOCK_ID (listed as -1); a rank needing more
+ * than max_blocks blocks -> DCP_DEV_ERR_TABLE (the list stops at max_blocks;
+ * totals still count every needed block).  workspace: its error word only
+ * (>= 256 bytes).  Asynchronous on `stream`.
+ */
+int dcp_transfer_blocks(const dcp_params* params, int32_t B, const int32_t* seq_lens,
+                        const int32_t* block_tables, int32_t max_blocks, int64_t num_blocks,
+                        int32_t* counts, int32_t* blocks, int32_t* fills, int64_t* totals,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Per-rank partial decode attention ("vLLM DCP and PCP", Deep Dive 6,
  * "Deriving the partial and global outputs"): for every virtual rank r,
  * request b, query token t and head h, with s_j = softmax_scale * q . k_j over

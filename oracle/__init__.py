@@ -10,6 +10,7 @@ Functions (all numpy in, numpy out):
   local_layout(L, N, I)                  (rank[L], local_pos[L]) by running count
   local_len(L, r, N, I)                  tokens of the first L that rank r owns
   slot_mapping(...)                      owner/slots/local_lens/virt/rank blocks
+  transfer_blocks(...)                   per-rank non-empty blocks, fills, totals
   attention(wl, rank=-1, rows=None)      (out [rows, Dv], lse [rows]) in fp64
   merge(o_parts, lse_parts)              exact LSE merge of per-rank partials
   decode(raw, dtype, scale)              stored values -> float64
@@ -45,6 +46,8 @@ def _load():
         lib.orc_decode.argtypes = [p, i64, i64, ctypes.c_double, p]
         lib.orc_slot_mapping.restype = ctypes.c_int
         lib.orc_slot_mapping.argtypes = [i64, i64, i64, i64, p, i64, p, p, p, i64, p, p, p, p, p]
+        lib.orc_transfer_blocks.restype = ctypes.c_int
+        lib.orc_transfer_blocks.argtypes = [i64, i64, i64, i64, p, p, i64, i64, p, p, p, p]
         lib.orc_attention.restype = None
         lib.orc_attention.argtypes = [i64, i64, i64, i64, i64, i64, i64, p, p, p, i64, p, p, i64,
                                       ctypes.c_double, ctypes.c_double, i64, i64, i64, i64, p, p, p, i64]
@@ -105,6 +108,22 @@ def slot_mapping(N, I, bs, seq_lens, tok_req, tok_pos, block_tables=None):
                                   _ptr(virt), _ptr(rblk))
     return dict(owner=owner[:T], slots=None if slots is None else slots[:, :T],
                 local_lens=local_lens[:, :B], virt_blocks=virt[:B], rank_blocks=rblk[:, :B], status=st)
+
+
+def transfer_blocks(N, I, bs, seq_lens, block_tables, num_blocks):
+    """Blocks moved under PD disaggregation.  Returns dict(counts [N, B],
+    blocks [N, B, max_blocks], fills [N, B, max_blocks], totals [2], status)."""
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    B = seq_lens.size
+    max_blocks = bt.shape[-1]
+    counts = np.empty((N, max(1, B)), dtype=np.int32)
+    blocks = np.empty((N, max(1, B), max_blocks), dtype=np.int32)
+    fills = np.empty((N, max(1, B), max_blocks), dtype=np.int32)
+    totals = np.zeros(2, dtype=np.int64)
+    st = _load().orc_transfer_blocks(N, I, bs, B, _ptr(seq_lens), _ptr(bt), max_blocks, int(num_blocks),
+                                     _ptr(counts), _ptr(blocks), _ptr(fills), _ptr(totals))
+    return dict(counts=counts[:, :B], blocks=blocks[:, :B], fills=fills[:, :B], totals=totals, status=st)
 
 
 def attention(wl, rank=-1, rows=None, nthreads=None):

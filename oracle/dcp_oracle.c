@@ -21,6 +21,9 @@
  *    "Virtual Block");
  *  - slot = block_table[rank][req][lpos / bs] * bs + lpos % bs for the owner,
  *    -1 for every other rank (section 2, slot-mapping figure text: -1 = skip);
+ *  - blocks moved under prefill-decode disaggregation: the blocks that hold
+ *    at least one token, with their token counts (section 2, "Practical
+ *    considerations for PD disaggregation");
  *  - attention of one query row against a token set K:
  *      s_j = scale * q . k_j,  L = log sum_j exp(s_j),
  *      o = sum_j exp(s_j) v_j / exp(L)   ("vLLM DCP and PCP", Deep Dive 6,
@@ -192,6 +195,62 @@ int orc_slot_mapping(int64_t N, int64_t I, int64_t bs, int64_t B, const int32_t*
     free(first);
     free(order);
     free(fill);
+    return status;
+}
+
+/*
+ * Blocks moved under prefill-decode disaggregation ("Breaking the
+ * Long-Sequence Inference Bottleneck ...", section 2, "Practical
+ * considerations for PD disaggregation": KV moves between nodes in whole
+ * blocks, and a block that holds no token need not move).  By enumeration:
+ * walk every token of each request, put it in its owner's local block
+ * lpos / bs, count the tokens per (rank, local block), and list each rank's
+ * local blocks that hold at least one token, in block-table order.
+ *   counts[N][B]              listed blocks
+ *   blocks[N][B][max_blocks]  their ids, -1 after the last
+ *   fills[N][B][max_blocks]   their token counts, 0 after the last
+ *   totals[2]                 {sum of counts * bs (slots moved), sum of tokens}
+ * Returns 0, or -1 if a listed block's table entry lies outside
+ * [0, num_blocks) (listed as -1) or a rank needs more than max_blocks blocks
+ * (the list stops at max_blocks).
+ */
+int orc_transfer_blocks(int64_t N, int64_t I, int64_t bs, int64_t B, const int32_t* seq_lens,
+                        const int32_t* block_tables, int64_t max_blocks, int64_t num_blocks,
+                        int32_t* counts, int32_t* blocks, int32_t* fills, int64_t* totals) {
+    int status = 0;
+    totals[0] = 0;
+    totals[1] = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t L = seq_lens[b] > 0 ? seq_lens[b] : 0;
+        int64_t nblk = L / bs + 2;  /* local blocks any rank could touch */
+        int64_t* tally = (int64_t*)calloc((size_t)(N * nblk), sizeof(int64_t));
+        int32_t* rank = (int32_t*)malloc((size_t)(L > 0 ? L : 1) * sizeof(int32_t));
+        int64_t* lpos = (int64_t*)malloc((size_t)(L > 0 ? L : 1) * sizeof(int64_t));
+        orc_local_layout(L, N, I, rank, lpos);
+        for (int64_t t = 0; t < L; ++t) tally[rank[t] * nblk + lpos[t] / bs]++;
+        for (int64_t r = 0; r < N; ++r) {
+            int32_t* ob = blocks + (r * B + b) * max_blocks;
+            int32_t* of = fills + (r * B + b) * max_blocks;
+            for (int64_t k = 0; k < max_blocks; ++k) { ob[k] = -1; of[k] = 0; }
+            int64_t c = 0;
+            for (int64_t k = 0; k < nblk; ++k) {
+                int64_t n = tally[r * nblk + k];
+                if (n == 0) continue;
+                totals[1] += n;
+                totals[0] += bs;
+                if (c >= max_blocks || k >= max_blocks) { status = -1; continue; }
+                int32_t id = block_tables[(r * B + b) * max_blocks + k];
+                if (id < 0 || id >= num_blocks) { status = -1; id = -1; }
+                ob[c] = id;
+                of[c] = (int32_t)n;
+                ++c;
+            }
+            counts[r * B + b] = (int32_t)c;
+        }
+        free(tally);
+        free(rank);
+        free(lpos);
+    }
     return status;
 }
 

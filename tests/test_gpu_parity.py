@@ -194,3 +194,64 @@ def test_token_outside_request_detected():
                          slots=slots, workspace=dw.workspace)
     assert dw.error_bits() & 0x2
     assert (slots == -1).all() and (owner == -1).all()
+
+
+# ------------------------------------------------------- PD block transfer
+
+def _transfer(dw, bt=None, num_blocks=None):
+    import context_decode_attention_gb300 as dcp
+    bt = dw.block_tables if bt is None else bt
+    N, B, M = bt.shape
+    counts = torch.full((N, B), -7, dtype=torch.int32, device="cuda")
+    blocks = torch.full((N, B, M), -7, dtype=torch.int32, device="cuda")
+    fills = torch.full((N, B, M), -7, dtype=torch.int32, device="cuda")
+    totals = torch.full((2,), -7, dtype=torch.int64, device="cuda")
+    dcp.dcp_transfer_blocks(dw.params, dw.seq_lens, bt, dw.num_blocks if num_blocks is None else num_blocks,
+                            counts, blocks, fills, totals, workspace=dw.workspace)
+    return [t.cpu().numpy() for t in (counts, blocks, fills, totals)]
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_transfer_blocks_bit_exact(name):
+    wl, dw = _setup(name)
+    c = wl.cfg
+    ref = oracle.transfer_blocks(int(c["N"]), int(c["I"]), int(c["block_size"]), wl.seq_lens,
+                                 dw.block_tables_host, dw.num_blocks)
+    assert ref["status"] == 0
+    counts, blocks, fills, totals = _transfer(dw)
+    assert np.array_equal(counts, ref["counts"])
+    assert np.array_equal(blocks, ref["blocks"])
+    assert np.array_equal(fills, ref["fills"])
+    assert np.array_equal(totals, ref["totals"])
+    assert dw.error_bits() == 0
+
+
+def test_transfer_blocks_errors_match_oracle():
+    wl, dw = _setup("gqa_bf16_ragged")
+    c = wl.cfg
+    N, I, bs = int(c["N"]), int(c["I"]), int(c["block_size"])
+    host = dw.block_tables_host.copy()
+    host[1, 0, 0] = dw.num_blocks + 3            # a listed entry outside the pool
+    ref = oracle.transfer_blocks(N, I, bs, wl.seq_lens, host, dw.num_blocks)
+    assert ref["status"] == -1
+    counts, blocks, fills, totals = _transfer(dw, torch.from_numpy(host).cuda())
+    assert dw.error_bits() == 0x1
+    for got, key in zip((counts, blocks, fills, totals), ("counts", "blocks", "fills", "totals")):
+        assert np.array_equal(got, ref[key]), key
+    short = np.ascontiguousarray(dw.block_tables_host[:, :, :2])   # request 0 needs more than two blocks
+    ref = oracle.transfer_blocks(N, I, bs, wl.seq_lens, short, dw.num_blocks)
+    assert ref["status"] == -1
+    counts, blocks, fills, totals = _transfer(dw, torch.from_numpy(short).cuda())
+    assert dw.error_bits() == 0x4
+    for got, key in zip((counts, blocks, fills, totals), ("counts", "blocks", "fills", "totals")):
+        assert np.array_equal(got, ref[key]), key
+
+
+def test_transfer_blocks_empty_batch():
+    import context_decode_attention_gb300 as dcp
+    wl, dw = _setup("gqa_bf16_ragged")
+    totals = torch.full((2,), 9, dtype=torch.int64, device="cuda")
+    e = torch.empty(0, dtype=torch.int32, device="cuda")
+    dcp.dcp_transfer_blocks(dw.params, e, dw.block_tables[:, :0], dw.num_blocks, e, totals=totals,
+                            workspace=dw.workspace)
+    assert totals.tolist() == [0, 0] and dw.error_bits() == 0

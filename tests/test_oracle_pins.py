@@ -337,3 +337,76 @@ def test_merge_weights_by_lse():
     mo, ml = oracle.merge(o, l)
     assert np.allclose(mo, [[0.25, 0.75]], atol=1e-15)
     assert ml[0] == pytest.approx(math.log(4.0), abs=1e-15)
+
+
+# ------------------------------------------------------- PD block transfer
+
+def test_transfer_blocks_pd_example():
+    """Section 2 example of the PD-disaggregation page: 16 tokens, block size
+    16, four ranks.  Interleave 1 moves four blocks a quarter full; interleave
+    16 moves one full block and nothing from the other ranks."""
+    lines = _read("pd_block_fill.txt")
+    L, bs, N = (int(lines[i].split()[1]) for i in range(3))
+    tables = np.arange(N * 2, dtype=np.int32).reshape(N, 1, 2) + 100
+    for ln in lines[3:]:
+        head, nblocks, _ = ln.split("|")
+        I, *lens = map(int, head.split())
+        tb = oracle.transfer_blocks(N, I, bs, np.array([L]), tables, num_blocks=200)
+        assert tb["status"] == 0
+        assert tb["counts"][:, 0].tolist() == list(map(int, nblocks.split()))
+        for r in range(N):
+            c = int(tb["counts"][r, 0])
+            assert tb["fills"][r, 0, :c].tolist() == ([lens[r]] if c else [])
+            assert tb["blocks"][r, 0, :c].tolist() == tables[r, 0, :c].tolist()
+            assert tb["blocks"][r, 0, c:].tolist() == [-1] * (2 - c)
+        # slots moved and tokens moved: fill 25% at I=1, 100% at I=bs
+        assert tb["totals"].tolist() == ([64, 16] if I == 1 else [16, 16])
+
+
+@pytest.mark.parametrize("N,I,bs", [(1, 1, 16), (4, 1, 16), (4, 16, 16), (3, 5, 8), (8, 64, 64), (2, 100, 16)])
+def test_transfer_blocks_invariants(N, I, bs):
+    """Fills add up to the request's length; every listed block is full but
+    the rank's last; the list is the table's first ceil(local_len / bs)
+    entries; totals are the sums.  Checked against the closed-form local
+    length, not the enumeration the oracle uses."""
+    seq_lens = np.array([0, 1, 15, 16, 17, 100, 1000, 4097], dtype=np.int32)
+    sm = oracle.slot_mapping(N, I, bs, seq_lens, np.zeros(0, np.int32), np.zeros(0, np.int64))
+    tables, nblk = allocate_blocks(sm["rank_blocks"], seed=3, spare=2)
+    tb = oracle.transfer_blocks(N, I, bs, seq_lens, tables, nblk)
+    assert tb["status"] == 0
+    slots = toks = 0
+    for b, L in enumerate(seq_lens.tolist()):
+        assert int(tb["fills"][:, b].sum()) == L
+        for r in range(N):
+            ln = oracle.local_len(L, r, N, I)
+            c = int(tb["counts"][r, b])
+            assert c == -(-ln // bs)
+            f = tb["fills"][r, b, :c]
+            assert np.all(f[:-1] == bs) and (c == 0 or 0 < f[-1] <= bs)
+            assert np.array_equal(tb["blocks"][r, b, :c], tables[r, b, :c])
+            assert np.all(tb["blocks"][r, b, c:] == -1) and np.all(tb["fills"][r, b, c:] == 0)
+            slots += c * bs
+            toks += ln
+    assert tb["totals"].tolist() == [slots, toks]
+
+
+def test_transfer_blocks_brute_force_tiny():
+    """Tiny case listed by hand: N=2, I=3, bs=4, L=14.  Tokens 0-2, 6-8, 12-13
+    go to rank 0 (8 tokens), 3-5, 9-11 to rank 1 (6 tokens)."""
+    tables = np.array([[[7, 3, 9]], [[2, 5, 0]]], dtype=np.int32)
+    tb = oracle.transfer_blocks(2, 3, 4, np.array([14]), tables, num_blocks=10)
+    assert tb["status"] == 0
+    assert tb["counts"][:, 0].tolist() == [2, 2]
+    assert tb["blocks"][:, 0].tolist() == [[7, 3, -1], [2, 5, -1]]
+    assert tb["fills"][:, 0].tolist() == [[4, 4, 0], [4, 2, 0]]
+    assert tb["totals"].tolist() == [16, 14]
+
+
+def test_transfer_blocks_reports_bad_tables():
+    tables = np.array([[[7, 30]], [[2, 5]]], dtype=np.int32)   # 30 is outside a 10-block pool
+    tb = oracle.transfer_blocks(2, 3, 4, np.array([14]), tables, num_blocks=10)
+    assert tb["status"] == -1 and tb["blocks"][0, 0].tolist() == [7, -1]
+    short = tables[:, :, :1].copy()                             # each rank needs two blocks
+    tb = oracle.transfer_blocks(2, 3, 4, np.array([14]), short, num_blocks=10)
+    assert tb["status"] == -1 and tb["counts"][:, 0].tolist() == [1, 1]
+    assert tb["totals"].tolist() == [16, 14]
