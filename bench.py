@@ -52,6 +52,9 @@ MEASURED_TRAFFIC = {
                              (219.009024e6 + 4.173568e6) / 376734),
     ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "6b7676725f33dc6503c889bff4fb6f14704e91ed09891ab0aba86be609714753",
                               (304.090624e6 + 4.698112e6) / 262144),
+    # per table entry (N B max_blocks) of the block-transfer listing
+    ("transfer_blocks", "entry"): ("transfer.cu", "b0688a22b3320dfa9866e87832949ba3d0d1442d4be44540bdf8d1b978a3fbb2",
+                                   (161.792e3 + 0.0) / (8 * 16 * 284)),
     ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "472cd388b3017692f89db1389a40a40652791550ac6d32b3e8a2fb95358a06ae",
                           (268.720128e6 + 3.707392e6) / 65536),
 }
@@ -302,6 +305,18 @@ def run_transfer(args):
     if dw.error_bits() != 0:
         raise SystemExit("device error bits set during the timed region")
     ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    # context for a latency-bound launch: the same event bracket around a
+    # one-element fill (a trivial kernel), after the same L2 flush
+    one = torch.zeros(1, dtype=torch.int32, device=dev)
+    fl = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for k in range(K):
+            flush.fill_(k & 255)
+            fl[k][0].record(stream)
+            one.fill_(k)
+            fl[k][1].record(stream)
+    torch.cuda.synchronize()
+    floor_ms = float(np.mean([a.elapsed_time(b) for a, b in fl]))
 
     # algorithmic bytes of one launch: the lengths and the listed table
     # entries read once; counts, blocks, fills and totals written once
@@ -348,9 +363,13 @@ def run_transfer(args):
         "blocks_listed": listed, "slots_moved": int(tot[0]), "tokens_moved": int(tot[1]),
         "transfer_fill": float(tot[1]) / max(1, int(tot[0])),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg_bytes,
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": measured_traffic("transfer_blocks", "entry", N * B * M),
+                     "traffic_note": "ncu DRAM bytes per table entry of one capture (profiles/), scaled to this launch",
+                     "algorithmic_bytes": alg_bytes,
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json, burst)",
                      "kernel": "transfer_blocks_kernel"},
+        "trivial_launch_ms": floor_ms,
         "gpu_launches": int(launches), "clocks": clk, "e2e": e2e, "parity": "bit-exact vs oracle",
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -271,10 +271,9 @@ int dcp_transfer_blocks(const dcp_params* params, int32_t B, const int32_t* seq_
         return DCP_OK;
     }
     if (!seq_lens || !block_tables || !counts || max_blocks < 1 || num_blocks < 1) return DCP_ERR_INVALID_ARG;
-    if (!aligned8(totals)) return DCP_ERR_INVALID_ARG;
+    if (!aligned8(totals) || (int64_t)p.N * B * max_blocks > INT32_MAX) return DCP_ERR_INVALID_ARG;
     return launch_transfer_blocks(p.N, p.I, p.block_size, B, max_blocks, num_blocks, seq_lens, block_tables,
-                                  counts, blocks, fills, totals, &reinterpret_cast<WsHeader*>(workspace)->err,
-                                  stream) == cudaSuccess
+                                  counts, blocks, fills, totals, workspace, stream) == cudaSuccess
                ? DCP_OK
                : DCP_ERR_CUDA;
 }

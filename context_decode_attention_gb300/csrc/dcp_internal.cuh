@@ -48,7 +48,12 @@ struct WsHeader {
     uint32_t err;
     uint32_t pad;
     int64_t total_chunks;
+    // block-transfer totals: per-block partials accumulate here, the last
+    // block to finish publishes them and puts both words back to zero
+    unsigned long long xfer_acc[2];
+    uint32_t xfer_done;
 };
+static_assert(sizeof(WsHeader) <= 256, "the workspace header is 256 bytes");
 
 struct WsLayout {
     size_t off_units, off_seg_base, off_counters, off_part_o, off_part_lse, off_qprep, total;
@@ -162,7 +167,7 @@ cudaError_t launch_attn_mla_f8(const AttnArgs& a, cudaStream_t s);
 // blocks moved under prefill-decode disaggregation (dcp_transfer_blocks)
 cudaError_t launch_transfer_blocks(int N, int I, int bs, int B, int max_blocks, int64_t num_blocks,
                                    const int32_t* seq_lens, const int32_t* block_tables, int32_t* counts,
-                                   int32_t* blocks, int32_t* fills, int64_t* totals, uint32_t* err,
+                                   int32_t* blocks, int32_t* fills, int64_t* totals, void* workspace,
                                    cudaStream_t s);
 
 // standalone merge for dcp_lse_merge

@@ -9,11 +9,34 @@
 // A rank stores its tokens in local-position order, so the blocks holding
 // tokens of request b on rank r are the first ceil(len / bs) entries of its
 // block table (len = the rank's local length), all full but the last, which
-// holds len - (count - 1) bs.  One thread per (rank, request, table entry).
+// holds len - (count - 1) bs.
+//
+// One thread per (rank, request, table entry), 32-bit index arithmetic, every
+// load of a thread issued at once (the launch is latency-bound: a few hundred
+// KB).  The batch totals are reduced per block and then across blocks through
+// two accumulators in the workspace header; the last block to finish
+// publishes them and zeroes the accumulators for the next call, so no
+// separate memset and no per-element atomics are needed.
 #include "dcp_internal.cuh"
 
 namespace dcp {
 namespace {
+
+constexpr int kThreads = 256, kWarps = kThreads / 32;
+
+// local_len for L < 2^31 with 32-bit divisions only (the period N I may
+// exceed 32 bits; then every token lies in the first period).
+__device__ __forceinline__ uint32_t local_len_u32(uint32_t L, int r, int N, int I) {
+    const uint64_t period = (uint64_t)N * (uint64_t)I;
+    uint32_t full = 0, rem = L;
+    if (period <= L) {
+        full = L / (uint32_t)period;
+        rem = L - full * (uint32_t)period;
+    }
+    int64_t extra = (int64_t)rem - (int64_t)r * I;
+    extra = extra < 0 ? 0 : (extra > I ? I : extra);
+    return full * (uint32_t)I + (uint32_t)extra;
+}
 
 struct TransferArgs {
     int N, I, bs, B, max_blocks;
@@ -23,41 +46,76 @@ struct TransferArgs {
     int32_t* counts;
     int32_t* blocks;
     int32_t* fills;
-    unsigned long long* totals;  // [2]: slots moved, tokens moved
-    uint32_t* err;
+    int64_t* totals;  // [2]: slots moved, tokens moved (optional)
+    WsHeader* hdr;
 };
 
-__global__ void transfer_blocks_kernel(TransferArgs a) {
-    const int64_t total = (int64_t)a.N * a.B * a.max_blocks;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int k = (int)(i % a.max_blocks);
-        const int64_t rb = i / a.max_blocks;  // r * B + b
-        const int b = (int)(rb % a.B), r = (int)(rb / a.B);
-        const int64_t L = a.seq_lens[b];
-        const int64_t len = L > 0 ? local_len(L, r, a.N, a.I) : 0;
-        const int64_t need = ceil_div64(len, a.bs);
-        const int64_t cnt = need < a.max_blocks ? need : a.max_blocks;
+__global__ void __launch_bounds__(kThreads) transfer_blocks_kernel(TransferArgs a) {
+    const uint32_t M = (uint32_t)a.max_blocks, B = (uint32_t)a.B;
+    const uint32_t total = (uint32_t)a.N * B * M;
+    unsigned long long slots = 0, toks = 0;  // this thread's share of the totals
+    for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < total; i += gridDim.x * kThreads) {
+        const uint32_t p = i / M, k = i - p * M;  // p = r * B + b
+        const uint32_t r = p / B, b = p - r * B;
+        // both loads are in bounds for every i, so they issue together; the
+        // table entry is used only when it is listed
+        const int32_t L = a.seq_lens[b];
+        const int32_t raw = a.block_tables[i];
+        const uint32_t len = L > 0 ? local_len_u32((uint32_t)L, (int)r, a.N, a.I) : 0u;
+        const uint32_t need = len / (uint32_t)a.bs + (len % (uint32_t)a.bs != 0);
+        const uint32_t cnt = need < M ? need : M;
         if (k == 0) {
-            if (need > a.max_blocks) raise_err(a.err, DCP_DEV_ERR_TABLE);
-            a.counts[rb] = (int32_t)cnt;
-            if (a.totals) {
-                atomicAdd(&a.totals[0], (unsigned long long)(need * a.bs));
-                atomicAdd(&a.totals[1], (unsigned long long)len);
-            }
+            if (need > M) raise_err(&a.hdr->err, DCP_DEV_ERR_TABLE);
+            a.counts[p] = (int32_t)cnt;
+            slots += (unsigned long long)need * (unsigned long long)a.bs;
+            toks += len;
         }
         int32_t id = -1, fill = 0;
         if (k < cnt) {
-            id = a.block_tables[i];
+            id = raw;
             if (id < 0 || id >= a.num_blocks) {
-                raise_err(a.err, DCP_DEV_ERR_BLOCK_ID);
+                raise_err(&a.hdr->err, DCP_DEV_ERR_BLOCK_ID);
                 id = -1;
             }
-            const int64_t rest = len - (int64_t)k * a.bs;
-            fill = (int32_t)(rest < a.bs ? rest : a.bs);
+            const uint32_t rest = len - k * (uint32_t)a.bs;  // k < cnt, so rest > 0
+            fill = (int32_t)(rest < (uint32_t)a.bs ? rest : (uint32_t)a.bs);
         }
         if (a.blocks) a.blocks[i] = id;
         if (a.fills) a.fills[i] = fill;
+    }
+    if (a.totals == nullptr) return;
+
+    for (int o = 16; o > 0; o >>= 1) {
+        slots += __shfl_xor_sync(0xffffffffu, slots, o);
+        toks += __shfl_xor_sync(0xffffffffu, toks, o);
+    }
+    __shared__ unsigned long long part[kWarps][2];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        part[warp][0] = slots;
+        part[warp][1] = toks;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long s = 0, t = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            s += part[w][0];
+            t += part[w][1];
+        }
+        if (s) atomicAdd(&a.hdr->xfer_acc[0], s);
+        if (t) atomicAdd(&a.hdr->xfer_acc[1], t);
+        __threadfence();
+        if (atomicAdd(&a.hdr->xfer_done, 1u) == gridDim.x - 1) {
+            __threadfence();
+            // atomic reads see every block's device-scope additions
+            const unsigned long long S = atomicAdd(&a.hdr->xfer_acc[0], 0ull);
+            const unsigned long long T = atomicAdd(&a.hdr->xfer_acc[1], 0ull);
+            a.totals[0] = (int64_t)S;
+            a.totals[1] = (int64_t)T;
+            a.hdr->xfer_acc[0] = 0;
+            a.hdr->xfer_acc[1] = 0;
+            a.hdr->xfer_done = 0;
+        }
     }
 }
 
@@ -65,23 +123,18 @@ __global__ void transfer_blocks_kernel(TransferArgs a) {
 
 cudaError_t launch_transfer_blocks(int N, int I, int bs, int B, int max_blocks, int64_t num_blocks,
                                    const int32_t* seq_lens, const int32_t* block_tables, int32_t* counts,
-                                   int32_t* blocks, int32_t* fills, int64_t* totals, uint32_t* err,
+                                   int32_t* blocks, int32_t* fills, int64_t* totals, void* workspace,
                                    cudaStream_t s) {
-    if (totals) {
-        cudaError_t e = cudaMemsetAsync(totals, 0, 2 * sizeof(int64_t), s);
-        if (e != cudaSuccess) return e;
-    }
     TransferArgs a;
     a.N = N; a.I = I; a.bs = bs; a.B = B; a.max_blocks = max_blocks; a.num_blocks = num_blocks;
     a.seq_lens = seq_lens; a.block_tables = block_tables; a.counts = counts; a.blocks = blocks; a.fills = fills;
-    a.totals = reinterpret_cast<unsigned long long*>(totals);
-    a.err = err;
+    a.totals = totals;
+    a.hdr = reinterpret_cast<WsHeader*>(workspace);
     const int64_t total = (int64_t)N * B * max_blocks;
-    const int threads = 256;
-    int64_t grid = (total + threads - 1) / threads;
-    if (grid > 4096) grid = 4096;
+    int64_t grid = (total + kThreads - 1) / kThreads;
+    if (grid > 152 * 8) grid = 152 * 8;
     if (grid < 1) grid = 1;
-    transfer_blocks_kernel<<<(unsigned)grid, threads, 0, s>>>(a);
+    transfer_blocks_kernel<<<(unsigned)grid, kThreads, 0, s>>>(a);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -190,8 +190,12 @@ int dcp_slot_mapping(const dcp_params* params, int32_t B, const int32_t* seq_len
  * dcp_slot_mapping.  Device checks: a listed table entry outside
  * [0, num_blocks) -> DCP_DEV_ERR_BLOCK_ID (listed as -1); a rank needing more
  * than max_blocks blocks -> DCP_DEV_ERR_TABLE (the list stops at max_blocks;
- * totals still count every needed block).  workspace: its error word only
- * (>= 256 bytes).  Asynchronous on `stream`.
+ * totals still count every needed block).  N * B * max_blocks must fit in
+ * int32 (else DCP_ERR_INVALID_ARG).
+ * workspace: its 256-byte header only (error word and the totals'
+ * accumulators, zeroed once by dcp_workspace_init and left zero by every
+ * call); calls sharing a workspace must be ordered on one stream.
+ * Asynchronous on `stream`.
  */
 int dcp_transfer_blocks(const dcp_params* params, int32_t B, const int32_t* seq_lens,
                         const int32_t* block_tables, int32_t max_blocks, int64_t num_blocks,

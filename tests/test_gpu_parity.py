@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from dcp_workloads import config, make_workload
+from dcp_workloads import allocate_blocks, config, make_workload
 
 from gpu_common import assert_close_rows, f64, tol_for
 
@@ -255,3 +255,39 @@ def test_transfer_blocks_empty_batch():
     dcp.dcp_transfer_blocks(dw.params, e, dw.block_tables[:, :0], dw.num_blocks, e, totals=totals,
                             workspace=dw.workspace)
     assert totals.tolist() == [0, 0] and dw.error_bits() == 0
+
+
+@pytest.mark.parametrize("N,I,bs,B", [(8, 16, 16, 3000), (3, 5, 8, 700), (1, 1, 64, 40)])
+def test_transfer_blocks_many_requests_and_repeated_calls(N, I, bs, B):
+    """More (rank, request) pairs than the grid holds warps (the grid-stride
+    path and the cross-block totals), and back-to-back calls on one workspace
+    (the totals' accumulators must come back to zero after every call)."""
+    import context_decode_attention_gb300 as dcp
+    rng = np.random.default_rng(B)
+    seq_lens = rng.integers(0, 600, size=B).astype(np.int32)
+    seq_lens[::7] = 0
+    cfg = config("gqa_llama8b", N=N, I=I, block_size=bs, B=B)
+    params = dcp.params_from_config(cfg)
+    sm = oracle.slot_mapping(N, I, bs, seq_lens, np.zeros(0, np.int32), np.zeros(0, np.int64))
+    tables, nblk = allocate_blocks(sm["rank_blocks"], seed=B, spare=5)
+    ref = oracle.transfer_blocks(N, I, bs, seq_lens, tables, nblk)
+    assert ref["status"] == 0
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    dcp.dcp_workspace_init(ws)
+    sl, bt = torch.from_numpy(seq_lens).cuda(), torch.from_numpy(tables).cuda()
+    M = tables.shape[-1]
+    for rep in range(3):
+        counts = torch.full((N, B), -7, dtype=torch.int32, device="cuda")
+        blocks = torch.full((N, B, M), -7, dtype=torch.int32, device="cuda")
+        fills = torch.full((N, B, M), -7, dtype=torch.int32, device="cuda")
+        totals = torch.full((2,), -7, dtype=torch.int64, device="cuda")
+        if rep == 1:   # no totals requested: the accumulators are left alone
+            dcp.dcp_transfer_blocks(params, sl, bt, nblk, counts, blocks, fills, None, workspace=ws)
+            totals = torch.from_numpy(ref["totals"]).cuda()
+        else:
+            dcp.dcp_transfer_blocks(params, sl, bt, nblk, counts, blocks, fills, totals, workspace=ws)
+        got = [t.cpu().numpy() for t in (counts, blocks, fills, totals)]
+        for g, key in zip(got, ("counts", "blocks", "fills", "totals")):
+            assert np.array_equal(g, ref[key]), (rep, key)
+    assert dcp.dcp_get_error(ws) == 0
+    assert not ws.cpu().numpy().any()  # the header's accumulators are back to zero
