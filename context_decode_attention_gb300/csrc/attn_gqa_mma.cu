@@ -233,28 +233,68 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
         if (lane == 0) prev = atomicAdd(&counters[group], 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev != (uint32_t)(nseg - 1)) return;
-        // last arriver: merge the group's nseg partials
+        // last arriver: merge the group's nseg partials.  It runs in the
+        // kernel's tail (a group's last segment usually ends a worker's range),
+        // so every load of it is made independent: 8 lanes per row, 4 rows per
+        // pass, each lane D/8 output columns as float4 and, per batch of 8
+        // segments, one segment's log-sum-exp; batches rescale online.
         __threadfence();
         const int64_t base = seg_base[group];
-        for (int row = 0; row < a.rows; ++row) {
-            float mx = -INFINITY;
-            for (int i = 0; i < nseg; ++i) mx = fmaxf(mx, __ldcg(&part_lse[(base + i) * a.rows + row]));
-            float sum = 0.f;
-            if (mx != -INFINITY)
-                for (int i = 0; i < nseg; ++i) sum += exp2f((__ldcg(&part_lse[(base + i) * a.rows + row]) - mx) * 1.4426950408889634f);
-            const float inv = (sum > 0.f) ? 1.f / sum : 0.f;
-            for (int d = lane; d < a.Dv; d += 32) {
-                float acc = 0.f;
-                if (mx != -INFINITY)
-                    for (int i = 0; i < nseg; ++i) {
-                        const float li = __ldcg(&part_lse[(base + i) * a.rows + row]);
-                        if (li == -INFINITY) continue;
-                        acc += exp2f((li - mx) * 1.4426950408889634f) *
-                               __ldcg(&part_o[((base + i) * a.rows + row) * a.Dv + d]);
+        constexpr int kLpr = 8, kCols = D / kLpr, kV4 = kCols / 4;
+        constexpr float kLog2e = 1.4426950408889634f;
+        const int q = lane & (kLpr - 1), lane0 = lane & ~(kLpr - 1);
+        for (int r0 = 0; r0 < a.rows; r0 += 32 / kLpr) {
+            const int row = r0 + lane / kLpr;
+            const bool live = row < a.rows;
+            float mx = -INFINITY, sum = 0.f;
+            float4 acc[kV4];
+#pragma unroll
+            for (int v = 0; v < kV4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i0 = 0; i0 < nseg; i0 += kLpr) {
+                const int i = i0 + q;
+                const float li = (live && i < nseg) ? __ldcg(&part_lse[(base + i) * a.rows + row]) : -INFINITY;
+                float bm = li;
+#pragma unroll
+                for (int o = 1; o < kLpr; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+                const float nm = fmaxf(mx, bm);
+                const float sc = (nm == -INFINITY) ? 1.f : exp2f((mx - nm) * kLog2e);
+                const float wi = (li == -INFINITY) ? 0.f : exp2f((li - nm) * kLog2e);
+                float ws = wi;
+#pragma unroll
+                for (int o = 1; o < kLpr; o <<= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+                sum = sum * sc + ws;
+#pragma unroll
+                for (int v = 0; v < kV4; ++v) {
+                    acc[v].x *= sc; acc[v].y *= sc; acc[v].z *= sc; acc[v].w *= sc;
+                }
+                const int nb = nseg - i0 < kLpr ? nseg - i0 : kLpr;
+#pragma unroll
+                for (int k = 0; k < kLpr; ++k) {
+                    const float wk = __shfl_sync(0xffffffffu, wi, lane0 | k);
+                    if (k < nb && live) {
+                        const float4* src = reinterpret_cast<const float4*>(
+                            &part_o[((base + i0 + k) * a.rows + row) * a.Dv + q * kCols]);
+#pragma unroll
+                        for (int v = 0; v < kV4; ++v) {
+                            const float4 x = __ldcg(src + v);
+                            acc[v].x += wk * x.x; acc[v].y += wk * x.y; acc[v].z += wk * x.z; acc[v].w += wk * x.w;
+                        }
                     }
-                write_final(row, d, acc * inv);
+                }
+                mx = nm;
             }
-            if (lane == 0) write_lse(row, (mx == -INFINITY) ? -INFINITY : mx + logf(sum));
+            if (live) {
+                const float inv = (sum > 0.f) ? 1.f / sum : 0.f;
+#pragma unroll
+                for (int v = 0; v < kV4; ++v) {
+                    const int d = q * kCols + 4 * v;
+                    write_final(row, d, acc[v].x * inv);
+                    write_final(row, d + 1, acc[v].y * inv);
+                    write_final(row, d + 2, acc[v].z * inv);
+                    write_final(row, d + 3, acc[v].w * inv);
+                }
+                if (q == 0) write_lse(row, (mx == -INFINITY) ? -INFINITY : mx + logf(sum));
+            }
         }
         if (lane == 0) counters[group] = 0;
     };
