@@ -20,6 +20,8 @@ constexpr int kTok = 8;  // tokens scored together
 template <int DKC, int DVC>
 __global__ void __launch_bounds__(128) attn_generic_kernel(AttnArgs a, int q_dtype, int kv_dtype) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();     // the plan
+    pdl_trigger();  // the segment merge may launch
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(a.ws);
     const int64_t P = hdr->total_chunks;
     if (P == 0) return;
@@ -200,8 +202,7 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(AttnArgs a, int q_dty
 template <int DKC, int DVC>
 cudaError_t launch_t(const AttnArgs& a, int q_dtype, int kv_dtype, cudaStream_t s) {
     dim3 grid((unsigned)a.W, (unsigned)((a.rows + kTileRows - 1) / kTileRows));
-    attn_generic_kernel<DKC, DVC><<<grid, 128, 0, s>>>(a, q_dtype, kv_dtype);
-    return cudaGetLastError();
+    return launch_pdl(attn_generic_kernel<DKC, DVC>, grid, dim3(128), 0, s, a, q_dtype, kv_dtype);
 }
 
 }  // namespace

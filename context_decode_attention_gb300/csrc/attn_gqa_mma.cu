@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t w = (int64_t)blockIdx.x * kWarps + warp;
+    pdl_wait();  // the plan
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(a.ws);
     const int64_t P = hdr->total_chunks;
     if (P == 0) return;
@@ -455,8 +456,7 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(gqa_mma_kernel<D, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)((a.W + kWarps - 1) / kWarps);
-    gqa_mma_kernel<D, NST><<<blocks, kWarps * 32, C::kSmem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(gqa_mma_kernel<D, NST>, dim3(blocks), dim3(kWarps * 32), C::kSmem, s, a);
 }
 
 }  // namespace

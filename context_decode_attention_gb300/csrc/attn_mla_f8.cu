@@ -159,11 +159,9 @@ __device__ __forceinline__ void split4(float p0, float p1, float p2, float p3, u
 // by 2^-e (e chosen so that its largest magnitude lies in (224, 448]) and
 // split into hi and lo; the row's scale 2^e goes to qscale.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) mla_f8_qprep_kernel(const uint16_t* __restrict__ q, int64_t nrows,
-                                                           uint8_t* __restrict__ qp, float* __restrict__ qscale) {
+__device__ __forceinline__ void qprep_row(const uint16_t* __restrict__ q, int64_t row, uint8_t* __restrict__ qp,
+                                          float* __restrict__ qscale) {
     const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (row >= nrows) return;
     const uint4* src = reinterpret_cast<const uint4*>(q + row * kDk);
     // 16-column groups g = lane and lane + 32 (36 groups)
     const bool two = lane + 32 < kDk / 16;
@@ -221,6 +219,18 @@ __global__ void __launch_bounds__(256) mla_f8_qprep_kernel(const uint16_t* __res
     }
 }
 
+// Launched right after the planner and run beside it (the query is an input
+// of the call, complete before the planner started); it waits for the
+// planner before exiting, so the attention kernel that waits for it also
+// sees the plan.
+__global__ void __launch_bounds__(256) mla_f8_qprep_kernel(const uint16_t* __restrict__ q, int64_t nrows,
+                                                           uint8_t* __restrict__ qp, float* __restrict__ qscale) {
+    pdl_trigger();
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row < nrows) qprep_row(q, row, qp, qscale);
+    pdl_wait();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     mla_f8_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_kv, const float* __restrict__ qscale) {
@@ -234,6 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = blockIdx.x & 1;    // value columns [256 half, 256 half + 256)
     const int64_t w = blockIdx.x >> 1;  // worker
     const int tq = blockIdx.y;          // query token
+    pdl_wait();                         // the plan and the prepared query
+    pdl_trigger();                      // the segment merge may launch
     uint32_t* err = &reinterpret_cast<WsHeader*>(a.ws)->err;
     const int64_t P = reinterpret_cast<const WsHeader*>(a.ws)->total_chunks;
     if (P == 0) return;
@@ -637,9 +649,9 @@ cudaError_t launch_attn_mla_f8(const AttnArgs& a, cudaStream_t s) {
     uint8_t* qp = a.ws + a.lay.off_qprep;
     float* qscale = reinterpret_cast<float*>(qp + align256((size_t)nrows * kQRowBytes));
     const int rows_per_block = 8;
-    mla_f8_qprep_kernel<<<(unsigned)((nrows + rows_per_block - 1) / rows_per_block), 32 * rows_per_block, 0, s>>>(
-        reinterpret_cast<const uint16_t*>(a.q), nrows, qp, qscale);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(mla_f8_qprep_kernel, dim3((unsigned)((nrows + rows_per_block - 1) / rows_per_block)),
+                               dim3(32 * rows_per_block), 0, s, reinterpret_cast<const uint16_t*>(a.q), nrows, qp,
+                               qscale);
     if (e != cudaSuccess) return e;
     CUtensorMap tq, tkv;
     if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, qp, kQRowBytes, (uint64_t)nrows, kQRowBytes, kSubCols,
@@ -652,8 +664,7 @@ cudaError_t launch_attn_mla_f8(const AttnArgs& a, cudaStream_t s) {
     e = cudaFuncSetAttribute(mla_f8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(2 * a.W), (unsigned)a.Tq);
-    mla_f8_kernel<<<grid, kThreads, kSmem, s>>>(a, tq, tkv, qscale);
-    return cudaGetLastError();
+    return launch_pdl(mla_f8_kernel, grid, dim3(kThreads), kSmem, s, a, tq, tkv, qscale);
 }
 
 }  // namespace dcp

@@ -113,6 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = blockIdx.x & 1;    // value columns [256 half, 256 half + 256)
     const int64_t w = blockIdx.x >> 1;  // worker
     const int tq = blockIdx.y;          // query token
+    pdl_wait();                         // the plan
+    pdl_trigger();                      // the segment merge may launch
     uint32_t* err = &reinterpret_cast<WsHeader*>(a.ws)->err;
     const int64_t P = reinterpret_cast<const WsHeader*>(a.ws)->total_chunks;
     if (P == 0) return;
@@ -514,8 +516,7 @@ cudaError_t launch_attn_mla_tc(const AttnArgs& a, int kv_dtype, cudaStream_t s) 
     cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(2 * a.W), (unsigned)a.Tq);
-    mla_tc_kernel<<<grid, kThreads, kSmem, s>>>(a, tq, tkv);
-    return cudaGetLastError();
+    return launch_pdl(mla_tc_kernel, grid, dim3(kThreads), kSmem, s, a, tq, tkv);
 }
 
 }  // namespace dcp

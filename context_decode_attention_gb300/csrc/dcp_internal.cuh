@@ -7,6 +7,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/dcp.h"
 
 namespace dcp {
@@ -77,6 +79,30 @@ __host__ inline WsLayout ws_layout(int64_t U, int64_t G, int64_t seg_max, int64_
 
 // Count kernel launches (dcp_launch_count).
 void count_launches(int n);
+
+// Programmatic dependent launch.  A kernel started by launch_pdl may begin
+// while the kernel before it on the stream is still running: every thread
+// calls pdl_wait() before it touches anything that kernel (or earlier work)
+// wrote, and before it exits, so that its own completion implies its
+// predecessor's.  pdl_trigger() lets the next launch_pdl kernel begin.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+__host__ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                       Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Raise device error bits.
 __device__ __forceinline__ void raise_err(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }

@@ -100,6 +100,7 @@ __device__ __forceinline__ void store_out4(void* out, int64_t idx, float4 v, int
 
 // One warp per (group, row): merges the group's segment partials.
 __global__ void segment_merge_kernel(AttnArgs a) {
+    pdl_wait();  // the attention kernel's partials
     const int lane = threadIdx.x & 31;
     const int64_t g = blockIdx.x;
     const int row = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -174,8 +175,7 @@ __global__ void lse_merge_kernel(int N, int64_t rows, int Dv, const float* o_par
 cudaError_t launch_segment_merge(const AttnArgs& a, cudaStream_t s) {
     if (a.Gn == 0) return cudaSuccess;
     dim3 grid((unsigned)a.Gn, (unsigned)((a.rows + 3) / 4));
-    segment_merge_kernel<<<grid, 128, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(segment_merge_kernel, grid, dim3(128), 0, s, a);
 }
 
 cudaError_t launch_lse_merge(int N, int64_t rows, int Dv, const float* o_parts, const float* lse_parts,

@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     int32_t* seg_base = reinterpret_cast<int32_t*>(a.ws + a.lay.off_seg_base);
     uint32_t* counters = reinterpret_cast<uint32_t*>(a.ws + a.lay.off_counters);
     const int tid = threadIdx.x;
+    pdl_trigger();  // the attention kernel (or the query preparation) may launch now
     if (tid == 0) carry = 0;
     __syncthreads();
 
