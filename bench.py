@@ -53,7 +53,7 @@ MEASURED_TRAFFIC = {
     ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "6b7676725f33dc6503c889bff4fb6f14704e91ed09891ab0aba86be609714753",
                               (304.090624e6 + 4.698112e6) / 262144),
     # per table entry (N B max_blocks) of the block-transfer listing
-    ("transfer_blocks", "entry"): ("transfer.cu", "b0688a22b3320dfa9866e87832949ba3d0d1442d4be44540bdf8d1b978a3fbb2",
+    ("transfer_blocks", "entry"): ("transfer.cu", "ba69fc5af5bf509387a4668d62e0fd322f75cc04daf9e1105750d478aee93893",
                                    (161.792e3 + 0.0) / (8 * 16 * 284)),
     ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "472cd388b3017692f89db1389a40a40652791550ac6d32b3e8a2fb95358a06ae",
                           (268.720128e6 + 3.707392e6) / 65536),

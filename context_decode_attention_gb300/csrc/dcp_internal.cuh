@@ -35,6 +35,19 @@ __host__ __device__ __forceinline__ int64_t local_len(int64_t L, int r, int N, i
     return (L / period) * I + extra;
 }
 __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// local_len for L < 2^31 with 32-bit divisions only (the period N I may
+// exceed 32 bits; then every token lies in the first period).
+__host__ __device__ __forceinline__ uint32_t local_len32(uint32_t L, int r, int N, int I) {
+    const uint64_t period = (uint64_t)N * (uint64_t)I;
+    uint32_t full = 0, rem = L;
+    if (period <= L) {
+        full = L / (uint32_t)period;
+        rem = L - full * (uint32_t)period;
+    }
+    int64_t extra = (int64_t)rem - (int64_t)r * I;
+    extra = extra < 0 ? 0 : (extra > I ? I : extra);
+    return full * (uint32_t)I + (uint32_t)extra;
+}
 
 // ---------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned):

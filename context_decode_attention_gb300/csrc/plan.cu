@@ -39,9 +39,14 @@ __device__ int64_t block_inclusive_scan(int64_t v, int64_t* warp_tot) {
     return v + before;
 }
 
+// Unit prefix entries also kept in shared memory for the group pass (the
+// rest are read back from the workspace).
+constexpr int kUnitSmem = 4096;
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     __shared__ int64_t warp_tot[32];
     __shared__ int64_t carry;
+    __shared__ int64_t us_s[kUnitSmem + 1];
     __shared__ int empty_list[kPlanThreads];
     __shared__ int n_empty;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
@@ -53,7 +58,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (tid == 0) carry = 0;
     __syncthreads();
 
-    // 1. chunks per unit, with the metadata checks
+    // 1. chunks per unit, with the metadata checks (32-bit closed forms:
+    // lengths are int32)
     for (int64_t base = 0; base < a.U; base += kPlanThreads) {
         const int64_t u = base + tid;
         int64_t c = 0;
@@ -61,24 +67,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             const int r = (int)(u % a.N);
             const int64_t bk = u / a.N;
             const int b = (int)(bk / a.Hkv);
-            const int64_t L = a.seq_lens[b];
+            const int32_t L = a.seq_lens[b];
+            const int32_t given = a.local_lens[(int64_t)r * a.B + b];
             if (L < a.Tq) {
                 raise_err(&hdr->err, DCP_DEV_ERR_TOKEN);
             } else {
-                int64_t n = a.local_lens[(int64_t)r * a.B + b];
-                const int64_t expect = local_len(L, r, a.N, a.I);
-                if (n != expect) raise_err(&hdr->err, DCP_DEV_ERR_STALE);
-                n = n < expect ? n : expect;
-                if (n < 0) n = 0;
-                if (ceil_div64(n, a.bs) > a.max_blocks) {
+                const uint32_t expect = local_len32((uint32_t)L, r, a.N, a.I);
+                if (given != (int32_t)expect) raise_err(&hdr->err, DCP_DEV_ERR_STALE);
+                uint32_t n = given < 0 ? 0u : ((uint32_t)given < expect ? (uint32_t)given : expect);
+                if (n / (uint32_t)a.bs + (n % (uint32_t)a.bs != 0) > (uint32_t)a.max_blocks) {
                     raise_err(&hdr->err, DCP_DEV_ERR_TABLE);
-                    n = (int64_t)a.max_blocks * a.bs;
+                    n = (uint32_t)a.max_blocks * (uint32_t)a.bs;
                 }
-                c = ceil_div64(n, a.CH);
+                c = n / (uint32_t)a.CH + (n % (uint32_t)a.CH != 0);
             }
         }
         const int64_t incl = block_inclusive_scan(c, warp_tot);
-        if (u < a.U) unit_start[u] = carry + incl - c;
+        if (u < a.U) {
+            unit_start[u] = carry + incl - c;
+            if (u <= kUnitSmem) us_s[u] = carry + incl - c;
+        }
         __syncthreads();
         if (tid == kPlanThreads - 1) carry += incl;
         __syncthreads();
@@ -86,43 +94,34 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     const int64_t P = carry;
     if (tid == 0) {
         unit_start[a.U] = P;
+        if (a.U <= kUnitSmem) us_s[a.U] = P;
         hdr->total_chunks = P;
+        carry = 0;
+        n_empty = 0;
     }
     __syncthreads();
-    if (tid == 0) carry = 0;
-    __syncthreads();
+    auto us_at = [&](int64_t i) -> int64_t { return i <= kUnitSmem ? us_s[i] : unit_start[i]; };
 
     // 2. segments per merge group.  With fewer chunks than workers only the
     // first P workers take part, so every worker in play owns >= 1 chunk.
+    // Groups that own no chunk (rare) get zeros and -inf.
     const int64_t We = P < a.W ? P : a.W;
     const int64_t per_group = a.partial_mode ? 1 : a.N;
+    const int G = a.Hq / a.Hkv;
     for (int64_t base = 0; base < a.G; base += kPlanThreads) {
         const int64_t g = base + tid;
         int64_t cnt = 0;
         if (g < a.G) {
-            const int64_t first = unit_start[g * per_group];
-            const int64_t end = unit_start[(g + 1) * per_group];
+            const int64_t first = us_at(g * per_group);
+            const int64_t end = us_at((g + 1) * per_group);
             if (end > first) cnt = worker_of(end - 1, We, P) - worker_of(first, We, P) + 1;
+            else empty_list[atomicAdd(&n_empty, 1)] = (int)tid;
             counters[g] = 0;
         }
         const int64_t incl = block_inclusive_scan(cnt, warp_tot);
         if (g < a.G) seg_base[g] = (int32_t)(carry + incl - cnt);
         __syncthreads();
         if (tid == kPlanThreads - 1) carry += incl;
-        __syncthreads();
-    }
-    if (tid == 0) seg_base[a.G] = (int32_t)carry;
-
-    // 3. groups that own no chunk (rare): zeros and -inf.  Each thread checks
-    // its groups and appends the empty ones to a shared list.
-    const int G = a.Hq / a.Hkv;
-    for (int64_t base = 0; base < a.G; base += kPlanThreads) {
-        if (tid == 0) n_empty = 0;
-        __syncthreads();
-        const int64_t g = base + tid;
-        if (g < a.G && unit_start[g * per_group] == unit_start[(g + 1) * per_group])
-            empty_list[atomicAdd(&n_empty, 1)] = (int)tid;
-        __syncthreads();
         for (int k = 0; k < n_empty; ++k) {
             const int64_t gg = base + empty_list[k];
             int b, kvh, r = 0;
@@ -150,7 +149,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             }
         }
         __syncthreads();
+        if (tid == 0) n_empty = 0;
+        __syncthreads();
     }
+    if (tid == 0) seg_base[a.G] = (int32_t)carry;
 }
 
 }  // namespace

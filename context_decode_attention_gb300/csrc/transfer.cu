@@ -24,20 +24,6 @@ namespace {
 
 constexpr int kThreads = 256, kWarps = kThreads / 32;
 
-// local_len for L < 2^31 with 32-bit divisions only (the period N I may
-// exceed 32 bits; then every token lies in the first period).
-__device__ __forceinline__ uint32_t local_len_u32(uint32_t L, int r, int N, int I) {
-    const uint64_t period = (uint64_t)N * (uint64_t)I;
-    uint32_t full = 0, rem = L;
-    if (period <= L) {
-        full = L / (uint32_t)period;
-        rem = L - full * (uint32_t)period;
-    }
-    int64_t extra = (int64_t)rem - (int64_t)r * I;
-    extra = extra < 0 ? 0 : (extra > I ? I : extra);
-    return full * (uint32_t)I + (uint32_t)extra;
-}
-
 struct TransferArgs {
     int N, I, bs, B, max_blocks;
     int64_t num_blocks;
@@ -61,7 +47,7 @@ __global__ void __launch_bounds__(kThreads) transfer_blocks_kernel(TransferArgs 
         // table entry is used only when it is listed
         const int32_t L = a.seq_lens[b];
         const int32_t raw = a.block_tables[i];
-        const uint32_t len = L > 0 ? local_len_u32((uint32_t)L, (int)r, a.N, a.I) : 0u;
+        const uint32_t len = L > 0 ? local_len32((uint32_t)L, (int)r, a.N, a.I) : 0u;
         const uint32_t need = len / (uint32_t)a.bs + (len % (uint32_t)a.bs != 0);
         const uint32_t cnt = need < M ? need : M;
         if (k == 0) {

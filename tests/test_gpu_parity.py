@@ -24,6 +24,8 @@ CASES = {
     "gqa_bf16_single_token": config("gqa_llama8b", B=3, lengths=("list", [1, 1, 2])),
     "gqa_bf16_d64": config("gqa_llama8b", B=2, Hq=8, Hkv=2, Dk=64, Dv=64, N=3, I=5, lengths=("list", [600, 91])),
     "gqa_fp8": config("gqa_llama8b", B=2, kv_dtype="fp8", lengths=("list", [400, 129])),
+    # more units (B x Hkv x N = 5120) than the planner keeps in shared memory
+    "gqa_bf16_many_units": config("gqa_llama8b", B=160, lengths=("lognormal", 40, 0.8, 1, 300)),
     "mla_bf16": config("mla_bf16_32k", B=2, lengths=("list", [700, 1531])),
     "mla_bf16_I64_short": config("mla_bf16_32k", B=2, lengths=("list", [100, 64])),
     "mla_fp8_mixed": config("mla_fp8_mixed", B=3, lengths=("list", [300, 1100, 77])),
