@@ -120,6 +120,32 @@ __host__ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3
 // Raise device error bits.
 __device__ __forceinline__ void raise_err(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
 
+// Chunks of unit u = ((b * Hkv + kvh) * N + r) with the plan's checks:
+// seq_len < Tq -> DCP_DEV_ERR_TOKEN (no chunk); a local length that differs
+// from the closed form -> DCP_DEV_ERR_STALE (the smaller one is used); more
+// blocks than max_blocks -> DCP_DEV_ERR_TABLE (clamped).  Errors are raised
+// only when `err` is non-null.  Lengths are int32, so 32-bit closed forms.
+__device__ __forceinline__ int64_t unit_chunks(int64_t u, int N, int I, int Hkv, int B, int Tq, int bs, int CH,
+                                               int max_blocks, const int32_t* seq_lens, const int32_t* local_lens,
+                                               uint32_t* err) {
+    const int r = (int)(u % N);
+    const int b = (int)((u / N) / Hkv);
+    const int32_t L = seq_lens[b];
+    const int32_t given = local_lens[(int64_t)r * B + b];
+    if (L < Tq) {
+        if (err) raise_err(err, DCP_DEV_ERR_TOKEN);
+        return 0;
+    }
+    const uint32_t expect = local_len32((uint32_t)L, r, N, I);
+    if (given != (int32_t)expect && err) raise_err(err, DCP_DEV_ERR_STALE);
+    uint32_t n = given < 0 ? 0u : ((uint32_t)given < expect ? (uint32_t)given : expect);
+    if (n / (uint32_t)bs + (n % (uint32_t)bs != 0) > (uint32_t)max_blocks) {
+        if (err) raise_err(err, DCP_DEV_ERR_TABLE);
+        n = (uint32_t)max_blocks * (uint32_t)bs;
+    }
+    return n / (uint32_t)CH + (n % (uint32_t)CH != 0);
+}
+
 // Which worker (of W over P chunks, worker w owning [w*P/W, (w+1)*P/W)) owns chunk x.
 __host__ __device__ __forceinline__ int64_t worker_of(int64_t x, int64_t W, int64_t P) {
     return ((x + 1) * W - 1) / P;

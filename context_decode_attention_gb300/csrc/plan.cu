@@ -58,30 +58,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (tid == 0) carry = 0;
     __syncthreads();
 
-    // 1. chunks per unit, with the metadata checks (32-bit closed forms:
-    // lengths are int32)
+    // 1. chunks per unit, with the metadata checks
     for (int64_t base = 0; base < a.U; base += kPlanThreads) {
         const int64_t u = base + tid;
-        int64_t c = 0;
-        if (u < a.U) {
-            const int r = (int)(u % a.N);
-            const int64_t bk = u / a.N;
-            const int b = (int)(bk / a.Hkv);
-            const int32_t L = a.seq_lens[b];
-            const int32_t given = a.local_lens[(int64_t)r * a.B + b];
-            if (L < a.Tq) {
-                raise_err(&hdr->err, DCP_DEV_ERR_TOKEN);
-            } else {
-                const uint32_t expect = local_len32((uint32_t)L, r, a.N, a.I);
-                if (given != (int32_t)expect) raise_err(&hdr->err, DCP_DEV_ERR_STALE);
-                uint32_t n = given < 0 ? 0u : ((uint32_t)given < expect ? (uint32_t)given : expect);
-                if (n / (uint32_t)a.bs + (n % (uint32_t)a.bs != 0) > (uint32_t)a.max_blocks) {
-                    raise_err(&hdr->err, DCP_DEV_ERR_TABLE);
-                    n = (uint32_t)a.max_blocks * (uint32_t)a.bs;
-                }
-                c = n / (uint32_t)a.CH + (n % (uint32_t)a.CH != 0);
-            }
-        }
+        const int64_t c = u < a.U ? unit_chunks(u, a.N, a.I, a.Hkv, a.B, a.Tq, a.bs, a.CH, a.max_blocks, a.seq_lens,
+                                                a.local_lens, &hdr->err)
+                                  : 0;
         const int64_t incl = block_inclusive_scan(c, warp_tot);
         if (u < a.U) {
             unit_start[u] = carry + incl - c;
