@@ -11,6 +11,7 @@ Functions (all numpy in, numpy out):
   local_len(L, r, N, I)                  tokens of the first L that rank r owns
   slot_mapping(...)                      owner/slots/local_lens/virt/rank blocks
   transfer_blocks(...)                   per-rank non-empty blocks, fills, totals
+  pcp_partition(K, ctx_lens, q_lens, max_q)  head-tail prefill partition
   attention(wl, rank=-1, rows=None)      (out [rows, Dv], lse [rows]) in fp64
   merge(o_parts, lse_parts)              exact LSE merge of per-rank partials
   decode(raw, dtype, scale)              stored values -> float64
@@ -46,6 +47,8 @@ def _load():
         lib.orc_decode.argtypes = [p, i64, i64, ctypes.c_double, p]
         lib.orc_slot_mapping.restype = ctypes.c_int
         lib.orc_slot_mapping.argtypes = [i64, i64, i64, i64, p, i64, p, p, p, i64, p, p, p, p, p]
+        lib.orc_pcp_partition.restype = ctypes.c_int
+        lib.orc_pcp_partition.argtypes = [i64, i64, p, p, i64, p, p]
         lib.orc_transfer_blocks.restype = ctypes.c_int
         lib.orc_transfer_blocks.argtypes = [i64, i64, i64, i64, p, p, i64, i64, p, p, p, p]
         lib.orc_attention.restype = None
@@ -124,6 +127,19 @@ def transfer_blocks(N, I, bs, seq_lens, block_tables, num_blocks):
     st = _load().orc_transfer_blocks(N, I, bs, B, _ptr(seq_lens), _ptr(bt), max_blocks, int(num_blocks),
                                      _ptr(counts), _ptr(blocks), _ptr(fills), _ptr(totals))
     return dict(counts=counts[:, :B], blocks=blocks[:, :B], fills=fills[:, :B], totals=totals, status=st)
+
+
+def pcp_partition(K, ctx_lens, q_lens, max_q):
+    """Head-tail prefill partition over K PCP ranks.  Returns dict(pos [B,
+    max_q] (global positions in gathered rank order, -1 = padding),
+    padded_len [B], status)."""
+    ctx = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    ql = np.ascontiguousarray(q_lens, dtype=np.int32)
+    B = ctx.size
+    pos = np.empty((max(1, B), max_q), dtype=np.int32)
+    plen = np.empty(max(1, B), dtype=np.int32)
+    st = _load().orc_pcp_partition(K, B, _ptr(ctx), _ptr(ql), max_q, _ptr(pos), _ptr(plen))
+    return dict(pos=pos[:B], padded_len=plen[:B], status=st)
 
 
 def attention(wl, rank=-1, rows=None, nthreads=None):

@@ -24,6 +24,11 @@
  *  - blocks moved under prefill-decode disaggregation: the blocks that hold
  *    at least one token, with their token counts (section 2, "Practical
  *    considerations for PD disaggregation");
+ *  - the prefill head-tail (zigzag) partition over K PCP ranks: pad to a
+ *    multiple of 2K, cut into 2K equal chunks, rank k takes chunks k and
+ *    2K - 1 - k ("Breaking the Long-Sequence Inference Bottleneck ...",
+ *    section 4, "Head-tail concatenation strategy" and the PCP Size = 2
+ *    walk-through);
  *  - attention of one query row against a token set K:
  *      s_j = scale * q . k_j,  L = log sum_j exp(s_j),
  *      o = sum_j exp(s_j) v_j / exp(L)   ("vLLM DCP and PCP", Deep Dive 6,
@@ -250,6 +255,47 @@ int orc_transfer_blocks(int64_t N, int64_t I, int64_t bs, int64_t B, const int32
         free(tally);
         free(rank);
         free(lpos);
+    }
+    return status;
+}
+
+/*
+ * Prefill context parallelism, head-tail partition ("Breaking the
+ * Long-Sequence Inference Bottleneck ...", section 4): request b's new tokens
+ * are the positions ctx_lens[b] .. ctx_lens[b] + q_lens[b] - 1.  Following
+ * the page's four steps: (1) align the count up to a multiple of 2K; (2) cut
+ * the aligned run into 2K equal chunks; (3) PCP rank k takes chunk k (head)
+ * and chunk 2K - 1 - k (tail); (4) rank k holds its head chunk followed by
+ * its tail chunk.  pos[b][0 .. max_q) receives every rank's tokens in rank
+ * order (rank 0's 2c positions, then rank 1's, ...: the order an AllGather of
+ * the ranks' queries leaves them in); an aligned position past the request's
+ * last token is padding, -1, as is every row past the aligned length.
+ * padded_len[b] = the aligned length.  Returns 0, or -1 if a request's
+ * aligned length exceeds max_q (its rows are then all -1).
+ */
+int orc_pcp_partition(int64_t K, int64_t B, const int32_t* ctx_lens, const int32_t* q_lens, int64_t max_q,
+                      int32_t* pos, int32_t* padded_len) {
+    int status = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        int32_t* row = pos + b * max_q;
+        for (int64_t j = 0; j < max_q; ++j) row[j] = -1;
+        const int64_t n = q_lens[b] > 0 ? q_lens[b] : 0;
+        const int64_t aligned = (n + 2 * K - 1) / (2 * K) * (2 * K); /* step 1 */
+        padded_len[b] = (int32_t)aligned;
+        if (aligned > max_q) {
+            status = -1;
+            continue;
+        }
+        const int64_t c = aligned / (2 * K); /* step 2: chunk i = [i c, (i + 1) c) */
+        int64_t out = 0;
+        for (int64_t k = 0; k < K; ++k) {
+            const int64_t chunks[2] = {k, 2 * K - 1 - k}; /* step 3 */
+            for (int h = 0; h < 2; ++h)                  /* step 4: head, then tail */
+                for (int64_t j = 0; j < c; ++j) {
+                    const int64_t rel = chunks[h] * c + j;
+                    row[out++] = rel < n ? (int32_t)(ctx_lens[b] + rel) : -1;
+                }
+        }
     }
     return status;
 }

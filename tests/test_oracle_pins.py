@@ -410,3 +410,43 @@ def test_transfer_blocks_reports_bad_tables():
     tb = oracle.transfer_blocks(2, 3, 4, np.array([14]), short, num_blocks=10)
     assert tb["status"] == -1 and tb["counts"][:, 0].tolist() == [1, 1]
     assert tb["totals"].tolist() == [16, 14]
+
+
+# ------------------------------------------------------ PCP head-tail partition
+
+def test_pcp_partition_page_examples():
+    for ln in _read("pcp_zigzag.txt"):
+        head, *ranks = ln.split("|")
+        K, n = map(int, head.split())
+        for ctx in (0, 37):
+            r = oracle.pcp_partition(K, [ctx], [n], n)
+            assert r["status"] == 0 and r["padded_len"].tolist() == [n]
+            per = n // K
+            for k, toks in enumerate(ranks):
+                want = [ctx + int(x) for x in toks.split()]
+                assert r["pos"][0, k * per:(k + 1) * per].tolist() == want
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4, 8])
+def test_pcp_partition_balances_causal_work(K):
+    """Aligned lengths: every rank's causal work (keys its queries see, with
+    the cached context in front) is the same, as the head-tail pairing intends;
+    rows form a permutation of the new positions."""
+    for n in [2 * K, 6 * K, 2 * K * 17]:
+        for ctx in [0, 1000]:
+            r = oracle.pcp_partition(K, [ctx], [n], n)
+            pos = r["pos"][0]
+            assert sorted(pos.tolist()) == list(range(ctx, ctx + n))
+            per = n // K
+            work = [int((pos[k * per:(k + 1) * per].astype(np.int64) + 1).sum()) for k in range(K)]
+            assert len(set(work)) == 1
+
+
+def test_pcp_partition_padding_and_overflow():
+    r = oracle.pcp_partition(2, [10, 0, 5], [5, 0, 4], 12)
+    assert r["status"] == 0 and r["padded_len"].tolist() == [8, 0, 4]
+    assert r["pos"][0].tolist() == [10, 11, -1, -1, 12, 13, 14, -1, -1, -1, -1, -1]
+    assert (r["pos"][1] == -1).all()
+    assert r["pos"][2].tolist()[:4] == [5, 8, 6, 7]
+    bad = oracle.pcp_partition(4, [0], [9], 8)   # aligned to 16 > 8 rows
+    assert bad["status"] == -1 and (bad["pos"] == -1).all()
