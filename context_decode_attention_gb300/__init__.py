@@ -6,7 +6,7 @@ build.py).  PyTorch supplies device memory and streams.  Nothing here falls
 back to the CPU: if the library is missing or cannot load, every call raises.
 
 Functions carry the C ABI's names (include/dcp.h):
-  dcp_workspace_size, dcp_workspace_init, dcp_get_error, dcp_slot_mapping, dcp_transfer_blocks,
+  dcp_workspace_size, dcp_workspace_init, dcp_get_error, dcp_slot_mapping, dcp_transfer_blocks, dcp_pcp_partition, dcp_prefill_attention,
   dcp_partial_attention, dcp_lse_merge, dcp_decode_attention
 """
 
@@ -20,7 +20,8 @@ from ._lib import (
 
 __all__ = [
     "DcpError", "DcpParams", "params_from_config", "lib", "lib_path",
-    "dcp_workspace_size", "dcp_workspace_init", "dcp_get_error", "dcp_slot_mapping", "dcp_transfer_blocks",
+    "dcp_workspace_size", "dcp_workspace_init", "dcp_get_error", "dcp_slot_mapping", "dcp_transfer_blocks", "dcp_pcp_partition",
+    "dcp_prefill_attention",
     "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention", "dcp_decode_attention_noalloc",
     "dcp_launch_count",
     "dcp_attention_kernel", "DCP_F32", "DCP_BF16", "DCP_FP8_E4M3", "DCP_LAYOUT_GQA", "DCP_LAYOUT_MLA",
@@ -112,6 +113,26 @@ def dcp_transfer_blocks(params, seq_lens, block_tables, num_blocks, counts, bloc
                                      _ptr(block_tables), int(block_tables.shape[-1]), int(num_blocks),
                                      _ptr(counts), _ptr(blocks), _ptr(fills), _ptr(totals), _ptr(workspace),
                                      _nbytes(workspace), _stream(stream)), "dcp_transfer_blocks")
+
+
+def dcp_pcp_partition(K, ctx_lens, q_lens, max_q, pos, padded_lens, workspace=None, stream=None):
+    """Head-tail prefill partition over K PCP ranks into pos [B, max_q] (gathered
+    order, -1 = padding) and padded_lens [B]; see include/dcp.h."""
+    _check(lib().dcp_pcp_partition(int(K), int(ctx_lens.numel()), _ptr(ctx_lens), _ptr(q_lens), int(max_q),
+                                   _ptr(pos), _ptr(padded_lens), _ptr(workspace), _nbytes(workspace),
+                                   _stream(stream)), "dcp_pcp_partition")
+
+
+def dcp_prefill_attention(params, q, q_pos, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens,
+                          out_partial, lse_partial, out=None, lse=None, workspace=None, stream=None):
+    """Causal prefill of gathered query rows q [B, Tq, Hq, D] at positions
+    q_pos [B, Tq]: per-rank partials, and the merged output when `out` is
+    given; see include/dcp.h."""
+    _check(lib().dcp_prefill_attention(ctypes.byref(params), int(q.shape[0]), int(q.shape[1]), _ptr(q), _ptr(q_pos),
+                                       _ptr(k_pool), _ptr(v_pool), int(num_blocks), _ptr(block_tables),
+                                       int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(local_lens),
+                                       _ptr(out_partial), _ptr(lse_partial), _ptr(out), _ptr(lse), _ptr(workspace),
+                                       _nbytes(workspace), _stream(stream)), "dcp_prefill_attention")
 
 
 def dcp_partial_attention(params, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens,

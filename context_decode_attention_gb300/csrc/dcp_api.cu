@@ -278,6 +278,55 @@ int dcp_transfer_blocks(const dcp_params* params, int32_t B, const int32_t* seq_
                : DCP_ERR_CUDA;
 }
 
+int dcp_pcp_partition(int32_t K, int32_t B, const int32_t* ctx_lens, const int32_t* q_lens, int32_t max_q,
+                      int32_t* pos, int32_t* padded_lens, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+    if (K < 1 || B < 0 || max_q < 0) return DCP_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < 256) return DCP_ERR_WORKSPACE;
+    if (B == 0) return DCP_OK;
+    if (!ctx_lens || !q_lens || !pos || !padded_lens) return DCP_ERR_INVALID_ARG;
+    if (max_q == 0) return DCP_ERR_INVALID_ARG;
+    return launch_pcp_partition(K, B, ctx_lens, q_lens, max_q, pos, padded_lens,
+                                &reinterpret_cast<WsHeader*>(workspace)->err, stream) == cudaSuccess
+               ? DCP_OK
+               : DCP_ERR_CUDA;
+}
+
+int dcp_prefill_attention(const dcp_params* params, int32_t B, int32_t Tq, const void* q, const int32_t* q_pos,
+                          const void* k_pool, const void* v_pool, int64_t num_blocks, const int32_t* block_tables,
+                          int32_t max_blocks, const int32_t* seq_lens, const int32_t* local_lens,
+                          float* out_partial, float* lse_partial, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+    int rc = validate_params(params);
+    if (rc != DCP_OK) return rc;
+    const dcp_params& p = *params;
+    if (B < 0 || Tq < 0) return DCP_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < 256) return DCP_ERR_WORKSPACE;
+    if (!prefill_supported(p)) return DCP_ERR_UNSUPPORTED;
+    if (B == 0 || Tq == 0) return DCP_OK;
+    if (!q || !q_pos || !k_pool || !v_pool || !block_tables || !seq_lens || !local_lens || !out_partial ||
+        !lse_partial)
+        return DCP_ERR_INVALID_ARG;
+    if (num_blocks < 1 || max_blocks < 1) return DCP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out_partial))
+        return DCP_ERR_INVALID_ARG;
+    PrefillArgs a;
+    memset(&a, 0, sizeof a);
+    a.N = p.N; a.I = p.I; a.bs = p.block_size; a.Hq = p.Hq; a.Hkv = p.Hkv; a.G = p.Hq / p.Hkv; a.D = p.Dk;
+    a.Tq = Tq; a.B = B; a.max_blocks = max_blocks; a.num_blocks = num_blocks; a.softmax_scale = p.softmax_scale;
+    a.q = q; a.q_pos = q_pos; a.k_pool = k_pool; a.v_pool = v_pool; a.block_tables = block_tables;
+    a.seq_lens = seq_lens; a.local_lens = local_lens; a.out_partial = out_partial; a.lse_partial = lse_partial;
+    a.ws = reinterpret_cast<uint8_t*>(workspace);
+    if (launch_prefill_partial(a, stream) != cudaSuccess) return DCP_ERR_CUDA;
+    count_launches(1);
+    if (out) {
+        if (launch_lse_merge(p.N, (int64_t)B * Tq * p.Hq, p.Dv, out_partial, lse_partial, out, p.out_dtype, lse,
+                             stream) != cudaSuccess)
+            return DCP_ERR_CUDA;
+    }
+    return DCP_OK;
+}
+
 int dcp_partial_attention(const dcp_params* params, int32_t B, const void* q, const void* k_pool,
                           const void* v_pool, int64_t num_blocks, const int32_t* block_tables,
                           int32_t max_blocks, const int32_t* seq_lens, const int32_t* local_lens,

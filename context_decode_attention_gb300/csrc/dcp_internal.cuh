@@ -205,6 +205,30 @@ struct AttnArgs {
     int rows;  // rows per group = Tq * G
 };
 
+// Causal prefill of a PCP-partitioned chunk: per-rank partials of query rows
+// with explicit global positions (GQA, bf16).
+struct PrefillArgs {
+    int N, I, bs, Hq, Hkv, G, D, Tq, B, max_blocks;
+    int64_t num_blocks;
+    float softmax_scale;
+    const void* q;           // [B][Tq][Hq][D]
+    const int32_t* q_pos;    // [B][Tq], -1 = padding
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const int32_t* local_lens;
+    float* out_partial;      // [N][B][Tq][Hq][D]
+    float* lse_partial;      // [N][B][Tq][Hq]
+    uint8_t* ws;
+};
+bool prefill_supported(const dcp_params& p);
+cudaError_t launch_prefill_partial(const PrefillArgs& a, cudaStream_t s);
+
+// head-tail prefill partition over K PCP ranks
+cudaError_t launch_pcp_partition(int K, int B, const int32_t* ctx_lens, const int32_t* q_lens, int max_q, int32_t* pos,
+                                 int32_t* padded_lens, uint32_t* err, cudaStream_t s);
+
 // generic CUDA-core path (any dtype / width); writes all segment partials,
 // then launch_segment_merge combines them.
 bool generic_supported(const dcp_params& p);

@@ -13,8 +13,8 @@ import torch
 from dcp_workloads import allocate_blocks
 
 from . import (
-    dcp_decode_attention, dcp_get_error, dcp_lse_merge, dcp_partial_attention, dcp_slot_mapping,
-    dcp_workspace_init, dcp_workspace_size, params_from_config,
+    dcp_decode_attention, dcp_get_error, dcp_lse_merge, dcp_partial_attention, dcp_pcp_partition,
+    dcp_prefill_attention, dcp_slot_mapping, dcp_workspace_init, dcp_workspace_size, params_from_config,
 )
 
 _TORCH_STORAGE = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8}
@@ -31,7 +31,7 @@ def raw_to_torch(arr, dtype):
 class DeviceWorkload:
     """A workload resident in HBM: q, paged KV pool, block tables, metadata."""
 
-    def __init__(self, wl, device="cuda:0", populate=True, spare_blocks=0, stream=None):
+    def __init__(self, wl, device="cuda:0", populate=True, spare_blocks=0, stream=None, workspace_bytes=None):
         self.wl = wl
         self.cfg = c = wl.cfg
         self.dev = torch.device(device)
@@ -43,7 +43,8 @@ class DeviceWorkload:
         self.mla = c["layout"] == "mla"
         dev = self.dev
         self.seq_lens = torch.from_numpy(wl.seq_lens.astype(np.int32)).to(dev)
-        self.ws_bytes = dcp_workspace_size(self.params, self.B, int(wl.seq_lens.max()))
+        # (prefill needs only the error word; the decode scratch grows with Tq)
+        self.ws_bytes = workspace_bytes or dcp_workspace_size(self.params, self.B, int(wl.seq_lens.max()))
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         dcp_workspace_init(self.workspace, self.stream)
 
@@ -136,6 +137,43 @@ class DeviceWorkload:
         dcp_lse_merge(self.N, rows, self.Dv, self.out_partial, self.lse_partial, out, self.params.out_dtype, lse,
                       self.stream)
         return out, lse
+
+    # -- prefill of the newest Tq tokens under PCP (head-tail partition) ---------
+    def prefill_setup(self, K):
+        """The chunk = every request's newest Tq tokens.  Runs the partition
+        over K PCP ranks once and lays the query rows out in the gathered
+        order (what an AllGather of the ranks' queries produces): an input
+        permutation, done once."""
+        B, Tq = self.B, self.Tq
+        self.pcp_K = int(K)
+        self.max_q = -(-Tq // (2 * self.pcp_K)) * 2 * self.pcp_K
+        self.ctx_lens = (self.seq_lens - Tq).to(torch.int32)
+        self.q_lens = torch.full((B,), Tq, dtype=torch.int32, device=self.dev)
+        self.q_pos = torch.empty((B, self.max_q), dtype=torch.int32, device=self.dev)
+        self.padded_lens = torch.empty(B, dtype=torch.int32, device=self.dev)
+        self.partition()
+        pos = self.q_pos.long()
+        natural = (pos - self.ctx_lens.long()[:, None]).clamp(min=0)
+        qg = torch.gather(self.q, 1, natural[:, :, None, None].expand(B, self.max_q, self.Hq, self.Dk))
+        self.q_gathered = torch.where((pos >= 0)[:, :, None, None], qg, torch.zeros_like(qg)).contiguous()
+        self.p_out = torch.empty((self.N, B, self.max_q, self.Hq, self.Dv), dtype=torch.float32, device=self.dev)
+        self.p_lse = torch.empty((self.N, B, self.max_q, self.Hq), dtype=torch.float32, device=self.dev)
+        ot = torch.float32 if self.cfg["out_dtype"] == "f32" else torch.bfloat16
+        self.g_out = torch.empty((B, self.max_q, self.Hq, self.Dv), dtype=ot, device=self.dev)
+        self.g_lse = torch.empty((B, self.max_q, self.Hq), dtype=torch.float32, device=self.dev)
+
+    def partition(self):
+        dcp_pcp_partition(self.pcp_K, self.ctx_lens, self.q_lens, self.max_q, self.q_pos, self.padded_lens,
+                          workspace=self.workspace, stream=self.stream)
+
+    def prefill(self, merged=True):
+        """One prefill attention pass: partition, per-rank causal partials, merge."""
+        self.partition()
+        dcp_prefill_attention(self.params, self.q_gathered, self.q_pos, self.k_pool, self.v_pool, self.num_blocks,
+                              self.block_tables, self.seq_lens, self.local_lens, self.p_out, self.p_lse,
+                              self.g_out if merged else None, self.g_lse if merged else None,
+                              workspace=self.workspace, stream=self.stream)
+        return self.g_out, self.g_lse
 
     def slot_mapping(self, tok_req, tok_pos):
         """owner / slots for given tokens (host arrays in, device tensors out)."""

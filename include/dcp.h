@@ -78,6 +78,7 @@ extern "C" {
 #define DCP_DEV_ERR_TABLE 0x4u      /* a rank needs more blocks than max_blocks */
 #define DCP_DEV_ERR_STALE 0x8u      /* local_lens disagree with seq_lens under (N, I) */
 #define DCP_DEV_ERR_TIMEOUT 0x10u   /* a bounded wait inside a kernel gave up */
+#define DCP_DEV_ERR_ROWS 0x20u      /* a request's padded prefill rows exceed the row capacity */
 
 typedef enum { DCP_F32 = 0, DCP_BF16 = 1, DCP_FP8_E4M3 = 2 } dcp_dtype;
 typedef enum { DCP_LAYOUT_GQA = 0, DCP_LAYOUT_MLA = 1 } dcp_layout;
@@ -201,6 +202,56 @@ int dcp_transfer_blocks(const dcp_params* params, int32_t B, const int32_t* seq_
                         const int32_t* block_tables, int32_t max_blocks, int64_t num_blocks,
                         int32_t* counts, int32_t* blocks, int32_t* fills, int64_t* totals,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Head-tail (zigzag) partition of prefill tokens over K PCP ranks ("Breaking
+ * the Long-Sequence Inference Bottleneck ...", section 4, "Head-tail
+ * concatenation strategy" and its PCP Size = 2 walk-through).  Request b's new
+ * tokens are the global positions ctx_lens[b] .. ctx_lens[b] + q_lens[b] - 1;
+ * their count is padded up to a multiple of 2K and cut into 2K equal chunks of
+ * c tokens; PCP rank k holds chunk k followed by chunk 2K - 1 - k.
+ *   pos[B][max_q]      (device int32) row j of request b in the gathered order
+ *                      (rank 0's 2c rows, then rank 1's, ...: the order an
+ *                      AllGather of the ranks' queries leaves them in): its
+ *                      global position, or -1 for padding (an aligned slot
+ *                      past the request's last token, or j >= the aligned
+ *                      length)
+ *   padded_lens[B]     (device int32) the aligned length of each request
+ * K >= 1; a request whose aligned length exceeds max_q gets all -1 rows and
+ * DCP_DEV_ERR_ROWS.  ctx_lens / q_lens: device int32 [B].  workspace: its
+ * error word only (>= 256 bytes).  Asynchronous on `stream`.
+ */
+int dcp_pcp_partition(int32_t K, int32_t B, const int32_t* ctx_lens, const int32_t* q_lens, int32_t max_q,
+                      int32_t* pos, int32_t* padded_lens, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+/*
+ * Causal prefill attention of PCP-gathered query rows against the DCP-sharded
+ * cache ("Breaking the Long-Sequence Inference Bottleneck ...", section 5,
+ * AllGather Q path: with the full query set, prefill is the DCP flow; "vLLM
+ * DCP and PCP", Deep Dive 6: per-rank partials and their exact LSE merge).
+ * Query row t of request b is q[b][t] ([B][Tq][Hq][Dk], the gathered order
+ * dcp_pcp_partition produces) at global position q_pos[b][t] (device int32,
+ * -1 = padding); it attends to the request's tokens 0 .. q_pos, which must
+ * already be in the cache (seq_lens[b] = cached tokens, including the chunk
+ * itself; a position >= seq_lens[b] raises DCP_DEV_ERR_TOKEN and the row is
+ * treated as padding).  For every virtual rank r:
+ *   out_partial[r][b][t][h][:]  (required, fp32) the rank's normalised partial
+ *   lse_partial[r][b][t][h]     (required, fp32) its natural-log LSE (-inf when
+ *                                the rank holds none of the row's tokens)
+ * and, when `out` is given, the merged output out[b][t][h][:] (params'
+ * out dtype) and lse[b][t][h] (optional).  Padding rows get zeros and -inf.
+ * Layouts, block tables, local lengths, device checks and workspace (error
+ * word only, >= 256 bytes) as for dcp_partial_attention; params->Tq is
+ * ignored (Tq is the row count here).  GQA, bf16 query and cache, Dk = Dv in
+ * {64, 128}, Hq / Hkv dividing 16; other combinations return
+ * DCP_ERR_UNSUPPORTED.  Asynchronous on `stream`.
+ */
+int dcp_prefill_attention(const dcp_params* params, int32_t B, int32_t Tq, const void* q, const int32_t* q_pos,
+                          const void* k_pool, const void* v_pool, int64_t num_blocks, const int32_t* block_tables,
+                          int32_t max_blocks, const int32_t* seq_lens, const int32_t* local_lens,
+                          float* out_partial, float* lse_partial, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Per-rank partial decode attention ("vLLM DCP and PCP", Deep Dive 6,
