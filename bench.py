@@ -48,15 +48,18 @@ def load_peaks():
 # the launch's cached tokens; summaries and commands under profiles/).  Valid
 # only for the kernel source they were taken on: a changed source gives null.
 MEASURED_TRAFFIC = {
-    ("mla_tcgen05", "fp8"): ("attn_mla_f8.cu", "e7e37847eb59021a5e349c2a40323bd8c63601405a2118c97056fb79a3c50c38",
-                             (219.009024e6 + 4.173568e6) / 376734),
-    ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "6b7676725f33dc6503c889bff4fb6f14704e91ed09891ab0aba86be609714753",
-                              (304.090624e6 + 4.698112e6) / 262144),
+    ("mla_tcgen05", "fp8"): ("attn_mla_f8.cu", "89621b2be7c25cbb7101401ea8e8bd2e47ea43b21fd4a9e344f0aa1d4ca210a4",
+                             (219.014144e6 + 3.834880e6) / 376734),
+    ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "b847f494ed1846da759188e5db92fa98126f116e61d13cc8cc7e44c5d41fc30a",
+                              (303.983104e6 + 4.574976e6) / 262144),
+    ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "55f1cce0d8111ec459e79dfdc0f0496849629421f35c1b418f54f7e664fe62df",
+                          (268.632576e6 + 3.230976e6) / 65536),
     # per table entry (N B max_blocks) of the block-transfer listing
     ("transfer_blocks", "entry"): ("transfer.cu", "ba69fc5af5bf509387a4668d62e0fd322f75cc04daf9e1105750d478aee93893",
                                    (161.792e3 + 0.0) / (8 * 16 * 284)),
-    ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "472cd388b3017692f89db1389a40a40652791550ac6d32b3e8a2fb95358a06ae",
-                          (268.720128e6 + 3.707392e6) / 65536),
+    # per request of the prefill workload's shape (2K chunk on a 64K context)
+    ("prefill", "request"): ("attn_prefill.cu", "26cd0da72bfc457f818172126161555cdabf17b9b5d19fe389ad783d0b8d8d95",
+                             295.139584e6 + 115.376896e6),
 }
 
 
@@ -389,6 +392,142 @@ def run_transfer(args):
         dist.destroy_process_group()
 
 
+PREFILL_METRIC = "PCP prefill: chunk tokens/s and tensor roofline (head-tail partition + causal prefill over DCP shards, 1 GB300)"
+
+
+def prefill_flops(wl):
+    """FLOPs of one prefill pass: every new token t of request b sees the
+    positions 0..p (p = L - Tq + t), 2 (Dk + Dv) per key and query head."""
+    c = wl.cfg
+    Tq, Hq, Dk, Dv = (int(c[k]) for k in ("Tq", "Hq", "Dk", "Dv"))
+    vis = sum(int(L) * Tq - Tq * (Tq - 1) // 2 for L in wl.seq_lens.astype(np.int64))
+    return 2 * vis * Hq * (Dk + Dv)
+
+
+def run_prefill(args):
+    """Time one PCP prefill step: the chunk's cache write, the head-tail
+    partition, causal prefill attention of the gathered rows over every
+    virtual rank's shard, and the LSE merge.  The KV (~0.55 GB) exceeds L2."""
+    import torch
+    import context_decode_attention_gb300 as dcp
+    from context_decode_attention_gb300.harness import DeviceWorkload
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name = args.workload if args.workload != DEFAULT_WORKLOAD else "gqa_prefill_64k"
+    over = {"B": args.batch} if args.batch else {}
+    if args.context:
+        over["L"] = args.context
+    cfg = config(name, **over)
+    wl = make_workload(cfg, seed=int(cfg["index"]) + 1000 * rank)
+    dw = DeviceWorkload(wl, device=dev, workspace_bytes=256)
+    K = int(cfg.get("pcp", 4))
+    dw.prefill_setup(K)
+    stream = dw.stream
+    peaks = load_peaks()
+    flops = prefill_flops(wl)
+    B, Tq = int(cfg["B"]), int(cfg["Tq"])
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            dw.write_new_tokens()
+            dw.prefill()
+    torch.cuda.synchronize()
+    if dw.error_bits() != 0:
+        raise SystemExit("device error bits set during warm-up")
+    steps = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = dcp.dcp_launch_count()
+    with torch.cuda.stream(stream):
+        for k in range(steps):
+            ev[k][0].record(stream)
+            dw.write_new_tokens()
+            ev[k][1].record(stream)
+            dw.prefill()
+            ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    launches = dcp.dcp_launch_count() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    if dw.error_bits() != 0:
+        raise SystemExit("device error bits set during the timed region")
+    step_ms = float(np.mean([e[0].elapsed_time(e[2]) for e in ev]))
+    attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    write_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+
+    e2e = None
+    if not args.no_e2e:
+        qg_h = dw.q_gathered.cpu().pin_memory()
+        nk_h, nv_h = dw.new_k.cpu().pin_memory(), dw.new_v.cpu().pin_memory()
+        out_h = torch.empty(dw.g_out.shape, dtype=dw.g_out.dtype).pin_memory()
+        lse_h = torch.empty(dw.g_lse.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (qg_h, nk_h, nv_h))
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                dw.q_gathered.copy_(qg_h, non_blocking=True)
+                dw.new_k.copy_(nk_h, non_blocking=True)
+                dw.new_v.copy_(nv_h, non_blocking=True)
+                dw.write_new_tokens()
+                dw.prefill()
+                out_h.copy_(dw.g_out, non_blocking=True)
+                lse_h.copy_(dw.g_lse, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max([e0.elapsed_time(e1) / steps], world)[0]
+        e2e = {"value": world * B * Tq / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+
+    step_ms, attn_ms, write_ms = reduce_max([step_ms, attn_ms, write_ms], world)
+    achieved = flops / (attn_ms / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"],
+            "traffic": measured_traffic("prefill", "request", B) if name == "gqa_prefill_64k" and not args.context else None,
+            "traffic_note": "ncu DRAM bytes of one request's launch (profiles/), times the requests",
+            "algorithmic_flops": flops,
+            "peak_source": peaks["source"] + " (MEASURED_PEAKS.json, burst; bf16 operands on mma.sync)",
+            "kernel": "prefill_partial_kernel", "attn_ms": attn_ms,
+            "roofline_ms": 1e3 * flops / (peaks["bf16_tflops"] * 1e12)}
+    line = {
+        "metric": PREFILL_METRIC, "value": world * B * Tq / (step_ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; a 2K-token chunk on a 64K cached context)",
+        "config": dict(workload_config(cfg, wl), op="prefill", pcp_ranks=K, chunk_tokens=Tq),
+        "cache_write_ms": write_ms, "roofline": roof, "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        c = wl.cfg
+        Hq = int(c["Hq"])
+        rows = np.arange(0, Hq * 8, dtype=np.int64) + (Tq - 8) * Hq  # the last 8 query tokens of request 0
+        threads = oracle.threads()
+        t0 = time.perf_counter()
+        oracle.attention(wl, rows=rows, nthreads=threads)
+        dt = time.perf_counter() - t0
+        per_flop = dt / (2 * len(rows) * int(wl.seq_lens[0]) * (int(c["Dk"]) + int(c["Dv"])))
+        line["cpu_baseline"] = {"value": B * Tq / (per_flop * flops), "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{len(rows)} query rows (the last 8 tokens x {Hq} heads of request 0), "
+                                          "fp64 C oracle, scaled by FLOPs to the whole step"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -400,14 +539,17 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling a smaller case)")
     ap.add_argument("--context", type=int, default=0, help="override to one fixed context length")
-    ap.add_argument("--op", default="decode", choices=["decode", "transfer-blocks"],
-                    help="decode: the decode step (default); transfer-blocks: the PD block-transfer listing")
+    ap.add_argument("--op", default="decode", choices=["decode", "transfer-blocks", "prefill"],
+                    help="decode: the decode step (default); transfer-blocks: the PD block-transfer listing; "
+                         "prefill: the PCP prefill step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         return run_reference(args)
     if args.op == "transfer-blocks":
         return run_transfer(args)
+    if args.op == "prefill":
+        return run_prefill(args)
 
     import torch
     import context_decode_attention_gb300 as dcp
