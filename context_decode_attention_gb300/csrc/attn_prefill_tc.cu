@@ -1,0 +1,412 @@
+// Causal prefill of PCP-gathered query rows against one DCP rank's shard on
+// tcgen05 tensor cores (kind::f16, bf16 in, fp32 accumulators in TMEM).
+//
+// What it computes is that of attn_prefill.cu ("Breaking the Long-Sequence
+// Inference Bottleneck ...", section 5, AllGather Q path; "vLLM DCP and
+// PCP", Deep Dive 6): every query row, at its own global position p, against
+// rank r's local positions below local_len(p + 1, r), as a normalised
+// partial with its LSE.  Here for D = 128 as a dense contraction:
+//
+//   CTA = 128 rows (128 / G query tokens x the G heads of one KV head) of one
+//   (request, KV head, rank); M = 128.  Q stays in shared memory (SW128,
+//   K-major).  K and V of 128 local tokens per tile go through a 3-stage
+//   ring; the cache's pages are block_size tokens, so producer warps copy
+//   them with 16-byte cp.async into the SW128 layout (zeros past the rows'
+//   furthest position) and publish each stage after a proxy fence.
+//   S = Q K^T (N = 128) lands in one of two TMEM buffers; the softmax warps
+//   (thread = row = TMEM lane) mask each row at its own bound, write P back
+//   as bf16 pairs over the buffer's first columns, and the P.V MMA reads it
+//   from TMEM (A operand) against V as an MN-major operand (N = 128 values).
+//   O (128 x 128 fp32) stays in TMEM; the reference max is lazy (O is
+//   rescaled only when a row's max grows by more than 2^8).
+//
+// Warps: 0-2 producers, 3 TMEM owner and MMA issuer (one lane), 4-7 softmax.
+// TMEM: O [0, 128), S buffers [128, 256) and [256, 384).  Every wait is
+// bounded; a timeout raises DCP_DEV_ERR_TIMEOUT and the role stops.
+#include "dcp_internal.cuh"
+#include "sm100_prims.cuh"
+
+namespace dcp {
+namespace {
+
+using namespace sm100;
+
+constexpr int kD = 128;
+constexpr int kRows = 128;                   // M
+constexpr int kKeys = 128;                   // local tokens per tile (N of QK)
+constexpr int kSub = 128 * 64 * 2;           // [128 rows x 64 bf16] SW128 sub-tile: 16 KB
+constexpr int kQBytes = 2 * kSub;            // 32 KB
+constexpr int kStageBytes = 4 * kSub;        // K (2 sub-tiles) + V (2 sub-tiles): 64 KB
+constexpr int kStages = 3;
+constexpr int kProd = 3;                     // producer warps
+constexpr int kProdThreads = 32 * kProd;
+constexpr int kWarpMma = kProd;
+constexpr int kWarpSoftmax = kWarpMma + 1;
+constexpr int kThreads = 32 * (kWarpSoftmax + 4);
+constexpr float kRescaleLog2 = 8.f;
+
+constexpr int kOffQ = 0;
+constexpr int kOffRing = kQBytes;
+constexpr int kOffBar = kOffRing + kStages * kStageBytes;
+constexpr int kNumBars = 2 * kStages + 1 + 2 + 2 + 1;
+constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
+static_assert(kSmem <= 232448, "shared memory");
+
+struct Bars {
+    uint64_t *full, *empty, *q_full, *s_full, *p_full, *o_done;
+    uint32_t* tmem_slot;
+};
+
+__device__ __forceinline__ Bars carve(uint8_t* base) {
+    uint64_t* b = reinterpret_cast<uint64_t*>(base + kOffBar);
+    Bars s;
+    s.full = b; b += kStages;
+    s.empty = b; b += kStages;
+    s.q_full = b++;
+    s.s_full = b; b += 2;
+    s.p_full = b; b += 2;
+    s.o_done = b++;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(b);
+    return s;
+}
+
+// byte offset of 16-byte chunk c16 (0..15) of row `row` in a [128 x 128 bf16]
+// tile stored as two SW128 sub-tiles of 64 columns
+__device__ __forceinline__ uint32_t sw128(int row, int c16) {
+    const int c = c16 & 7;
+    return (uint32_t)((c16 >> 3) * kSub + row * 128 + ((c ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool valid) {
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* sQ = smem + kOffQ;
+    uint8_t* sRing = smem + kOffRing;
+    const Bars sh = carve(smem);
+    __shared__ int s_kv;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    const int64_t nrt = ((int64_t)a.Tq * a.G + kRows - 1) / kRows;
+    const int64_t unit = blockIdx.x / nrt;
+    const int row0 = (int)(blockIdx.x % nrt) * kRows;
+    const int r = (int)(unit % a.N);
+    const int64_t bk = unit / a.N;
+    const int b = (int)(bk / a.Hkv), kvh = (int)(bk % a.Hkv);
+    uint32_t* err = &reinterpret_cast<WsHeader*>(a.ws)->err;
+
+    // rank r's local length of request b
+    const int32_t L = a.seq_lens[b];
+    int32_t len = 0;
+    if (L > 0) {
+        const uint32_t expect = local_len32((uint32_t)L, r, a.N, a.I);
+        const int32_t given = a.local_lens[(int64_t)r * a.B + b];
+        if (given != (int32_t)expect && threadIdx.x == 0) raise_err(err, DCP_DEV_ERR_STALE);
+        len = given < 0 ? 0 : ((uint32_t)given < expect ? given : (int32_t)expect);
+        if (((int64_t)len + a.bs - 1) / a.bs > a.max_blocks) {
+            if (threadIdx.x == 0) raise_err(err, DCP_DEV_ERR_TABLE);
+            len = a.max_blocks * a.bs;
+        }
+    }
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sh.full[i], kProdThreads);
+            mbar_init(&sh.empty[i], 1);
+        }
+        mbar_init(sh.q_full, 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sh.s_full[i], 1);
+            mbar_init(&sh.p_full[i], 4);
+        }
+        mbar_init(sh.o_done, 1);
+        fence_mbar_init();
+        s_kv = 0;
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(sh.tmem_slot, 512);
+        tmem_relinquish();
+    }
+    __syncthreads();  // barriers initialised, s_kv zeroed
+
+    // the softmax threads own the rows: position, causal bound, query row
+    const int h = threadIdx.x - 32 * kWarpSoftmax;  // row = TMEM lane (softmax warps)
+    int t_row = 0;
+    int32_t bound = 0;
+    if (warp >= kWarpSoftmax) {
+        const int row = row0 + h;
+        t_row = row / a.G;
+        if (t_row < a.Tq) {
+            const int32_t p = a.q_pos[(int64_t)b * a.Tq + t_row];
+            if (p >= L) raise_err(err, DCP_DEV_ERR_TOKEN);
+            else if (p >= 0) bound = min(len, (int32_t)local_len32((uint32_t)p + 1u, r, a.N, a.I));
+        }
+        atomicMax(&s_kv, bound);
+        // the query row into Q (SW128, K-major); rows past the request are zero
+        const uint4* src = nullptr;
+        if (t_row < a.Tq) {
+            const int gq = row % a.G;
+            src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                                 (((int64_t)b * a.Tq + t_row) * a.Hq + (int64_t)kvh * a.G + gq) * kD);
+        }
+#pragma unroll
+        for (int c16 = 0; c16 < 16; ++c16)
+            *reinterpret_cast<uint4*>(sQ + sw128(h, c16)) = src ? src[c16] : make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        mbar_arrive(sh.q_full);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *sh.tmem_slot;
+    const int kv = s_kv;
+    const int ntiles = (kv + kKeys - 1) / kKeys;
+
+    if (warp < kProd) {
+        // ------------------------------------------------------------ producers
+        const int pt = threadIdx.x;  // 0 .. 95
+        const int32_t* bt = a.block_tables + ((int64_t)r * a.B + b) * a.max_blocks;
+        const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k_pool);
+        const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v_pool);
+        const uint32_t ring = smem_u32(sRing);
+        bool alive = true, bad = false;
+        for (int t = 0; t < ntiles && alive; ++t) {
+            const int s = t % kStages;
+            if (lane == 0 && !mbar_wait_sleep(&sh.empty[s], ((t / kStages) & 1) ^ 1u)) alive = false;
+            alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
+            if (!alive) break;
+            const uint32_t st = ring + (uint32_t)s * kStageBytes;
+            for (int idx = pt; idx < kKeys * 16; idx += kProdThreads) {
+                const int row = idx >> 4, c16 = idx & 15;
+                const int lp = t * kKeys + row;
+                bool valid = lp < kv;
+                int64_t off = 0;
+                if (valid) {
+                    const int32_t blk = bt[lp / a.bs];
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        bad = true;
+                        valid = false;
+                    } else {
+                        off = ((((int64_t)blk * a.Hkv + kvh) * a.bs + lp % a.bs) * kD + c16 * 8) * 2;
+                    }
+                }
+                const uint32_t so = sw128(row, c16);
+                cp_async16_zfill(st + so, kp + off, valid);
+                cp_async16_zfill(st + 2 * kSub + so, vp + off, valid);
+            }
+            cp_async_commit();
+            if (t > 0) {
+                cp_async_wait<1>();
+                fence_proxy_async_smem();
+                mbar_arrive(&sh.full[(t - 1) % kStages]);
+            }
+        }
+        cp_async_wait<0>();
+        if (alive && ntiles > 0) {
+            fence_proxy_async_smem();
+            mbar_arrive(&sh.full[(ntiles - 1) % kStages]);
+        }
+        if (bad) raise_err(err, DCP_DEV_ERR_BLOCK_ID);
+        if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && ntiles > 0) {
+            bool alive = true;
+            const uint32_t idesc_qk = idesc_f16(1, kRows, kKeys, 0, 0);
+            const uint32_t idesc_pv = idesc_f16(1, kRows, kD, 0, 1);
+            const uint64_t dq = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSW128);
+            const uint64_t dring = smem_desc(smem_u32(sRing), 16, 1024, kLayoutSW128);
+            // values: MN-major, the two 64-column halves one sub-tile apart
+            const uint64_t dvr = smem_desc(smem_u32(sRing + 2 * kSub), kSub, 1024, kLayoutSW128);
+            constexpr uint32_t kSubDesc = kSub >> 4, kStageDesc = kStageBytes >> 4;
+            if (!mbar_wait_sleep(sh.q_full, 0)) alive = false;
+            auto pv = [&](int t) -> bool {
+                const int sb = t & 1;
+                if (!mbar_wait_sleep(&sh.p_full[sb], (t >> 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t pa = tm + 128 + 128 * sb;
+                const uint64_t vd = dvr + (uint64_t)(t % kStages) * kStageDesc;
+#pragma unroll 1
+                for (int kk = 0; kk < kKeys / 16; ++kk)
+                    mma_ts(tm, pa + 8 * kk, vd + 128 * kk, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&sh.empty[t % kStages]);
+                mma_commit(sh.o_done);
+                return true;
+            };
+            for (int t = 0; t < ntiles && alive; ++t) {
+                const int s = t % kStages;
+                if (!mbar_wait_sleep(&sh.full[s], (t / kStages) & 1)) { alive = false; break; }
+                tc_fence_after();
+                const uint32_t d = tm + 128 + 128 * (t & 1);
+                const uint64_t kd = dring + (uint64_t)s * kStageDesc;
+#pragma unroll 1
+                for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(d, dq + kc * kSubDesc + 2 * kk, kd + kc * kSubDesc + 2 * kk, idesc_qk,
+                               (kc | kk) != 0 ? 1u : 0u);
+                mma_commit(&sh.s_full[t & 1]);
+                if (t > 0 && !pv(t - 1)) { alive = false; break; }
+            }
+            if (alive && !pv(ntiles - 1)) alive = false;
+            if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warpgroup
+        const int quarter = warp & 3;
+        const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+        const float sl2 = a.softmax_scale * 1.4426950408889634f;
+        float m_ref = -INFINITY, l = 0.f;
+        bool alive = true;
+        // the tcgen05.ld / st below are warp-aligned: every wait's outcome is
+        // made uniform across the warp so that all lanes leave together
+        for (int t = 0; t < ntiles; ++t) {
+            const int sb = t & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&sh.s_full[sb], (t >> 1) & 1))) { alive = false; break; }
+            tc_fence_after();
+            const uint32_t sbase = tm + 128 + 128 * sb + lane_off;
+            // columns [0, lim) of this tile are visible to the row
+            const int lim = max(0, min(kKeys, bound - t * kKeys));
+            float mraw = -INFINITY;
+            {
+                uint32_t rr[32];
+#pragma unroll 1
+                for (int c = 0; c < kKeys / 32; ++c) {
+                    tmem_ld32(sbase + 32 * c, rr);
+                    tmem_wait_ld();
+                    const int lc = lim - 32 * c;
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        m4[k & 3] = fmaxf(m4[k & 3], (k < lc) ? __uint_as_float(rr[k]) : -INFINITY);
+                    mraw = fmaxf(mraw, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                }
+            }
+            const float mx = (lim > 0) ? mraw * sl2 : -INFINITY;
+            float corr = 1.f;
+            bool rescale_o = false;
+            if (mx > -INFINITY) {
+                if (m_ref == -INFINITY) {
+                    m_ref = mx;  // first visible tokens of the row: O holds zeros
+                    corr = 0.f;
+                } else if (mx > m_ref + kRescaleLog2) {
+                    corr = ex2_approx(m_ref - mx);
+                    m_ref = mx;
+                    rescale_o = true;
+                }
+            }
+            const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            float lsum = 0.f;
+#pragma unroll 1
+            for (int q = 0; q < kKeys / 16; ++q) {
+                uint32_t r16[16], pk[8];
+                tmem_ld16(sbase + 16 * q, r16);
+                tmem_wait_ld();
+                const int lq = lim - 16 * q;
+                float ls2[2] = {0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float s0 = (2 * k < lq) ? __uint_as_float(r16[2 * k]) : -INFINITY;
+                    const float s1 = (2 * k + 1 < lq) ? __uint_as_float(r16[2 * k + 1]) : -INFINITY;
+                    const float p0 = ex2_approx(fmaf(s0, sl2, nmu)), p1 = ex2_approx(fmaf(s1, sl2, nmu));
+                    ls2[0] += p0;
+                    ls2[1] += p1;
+                    pk[k] = pack_bf16(p0, p1);
+                }
+                lsum += ls2[0] + ls2[1];
+                tmem_st8(sbase + 8 * q, pk);
+            }
+            l = (corr == 0.f ? 0.f : l * corr) + lsum;
+            // P.V of the previous tile must be complete before O is touched
+            if (t > 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(sh.o_done, (t - 1) & 1))) { alive = false; break; }
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, rescale_o)) {
+                const float f = rescale_o ? corr : 1.f;
+                uint32_t ov[32];
+#pragma unroll 1
+                for (int i = 0; i < kD / 32; ++i) {
+                    tmem_ld32(tm + lane_off + 32 * i, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * f);
+                    tmem_st32(tm + lane_off + 32 * i, ov);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.p_full[sb]);
+        }
+        // epilogue: the last P.V, then the row's normalised partial and LSE
+        if (alive && ntiles > 0) {
+            if (!__all_sync(0xffffffffu, mbar_wait(sh.o_done, (ntiles - 1) & 1))) alive = false;
+            tc_fence_after();
+        }
+        // every lane reads its TMEM lane (rows past the request too: the load
+        // is warp-aligned); only the request's rows are written
+        const bool row_ok = t_row < a.Tq;
+        const bool read_o = alive && ntiles > 0;  // uniform across the warp
+        const bool has = read_o && l > 0.f;
+        const float inv = has ? 1.f / l : 0.f;
+        int64_t prow = 0;
+        if (row_ok) {
+            const int gq = (row0 + h) % a.G;
+            prow = (((int64_t)r * a.B + b) * a.Tq + t_row) * a.Hq + (int64_t)kvh * a.G + gq;
+        }
+        float* dst = a.out_partial + prow * kD;
+        uint32_t ov[32];
+#pragma unroll 1
+        for (int i = 0; i < kD / 32; ++i) {
+            if (read_o) {
+                tmem_ld32(tm + lane_off + 32 * i, ov);
+                tmem_wait_ld();
+            }
+            if (row_ok) {
+#pragma unroll
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4*>(dst + 32 * i + k) =
+                        has ? make_float4(__uint_as_float(ov[k]) * inv, __uint_as_float(ov[k + 1]) * inv,
+                                          __uint_as_float(ov[k + 2]) * inv, __uint_as_float(ov[k + 3]) * inv)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        if (row_ok) a.lse_partial[prow] = has ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        if (!alive && lane == 0) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma) tmem_dealloc(tm, 512);
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const PrefillArgs& a) {
+    return a.D == kD && a.G >= 1 && kRows % a.G == 0;
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t ctas = ((int64_t)a.Tq * a.G + kRows - 1) / kRows * ((int64_t)a.B * a.Hkv * a.N);
+    return launch_pdl(prefill_tc_kernel, dim3((unsigned)ctas), dim3(kThreads), kSmem, s, a);
+}
+
+}  // namespace dcp

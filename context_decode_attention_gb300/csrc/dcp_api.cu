@@ -317,7 +317,8 @@ int dcp_prefill_attention(const dcp_params* params, int32_t B, int32_t Tq, const
     a.q = q; a.q_pos = q_pos; a.k_pool = k_pool; a.v_pool = v_pool; a.block_tables = block_tables;
     a.seq_lens = seq_lens; a.local_lens = local_lens; a.out_partial = out_partial; a.lse_partial = lse_partial;
     a.ws = reinterpret_cast<uint8_t*>(workspace);
-    if (launch_prefill_partial(a, stream) != cudaSuccess) return DCP_ERR_CUDA;
+    if ((prefill_tc_supported(a) ? launch_prefill_tc(a, stream) : launch_prefill_partial(a, stream)) != cudaSuccess)
+        return DCP_ERR_CUDA;
     count_launches(1);
     if (out) {
         if (launch_lse_merge(p.N, (int64_t)B * Tq * p.Hq, p.Dv, out_partial, lse_partial, out, p.out_dtype, lse,

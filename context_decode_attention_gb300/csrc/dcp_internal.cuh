@@ -223,7 +223,9 @@ struct PrefillArgs {
     uint8_t* ws;
 };
 bool prefill_supported(const dcp_params& p);
-cudaError_t launch_prefill_partial(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_partial(const PrefillArgs& a, cudaStream_t s);  // mma.sync, D 64 / 128
+bool prefill_tc_supported(const PrefillArgs& a);                          // tcgen05, D 128
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 
 // head-tail prefill partition over K PCP ranks
 cudaError_t launch_pcp_partition(int K, int B, const int32_t* ctx_lens, const int32_t* q_lens, int max_q, int32_t* pos,
