@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         __syncthreads();
     }
     const int64_t P = carry;
+    __syncthreads();  // every thread holds the total before carry is reused
     if (tid == 0) {
         unit_start[a.U] = P;
         if (a.U <= kUnitSmem) us_s[a.U] = P;
