@@ -10,9 +10,14 @@
 //   CTA = 128 rows (128 / G query tokens x the G heads of one KV head) of one
 //   (request, KV head, rank); M = 128.  Q stays in shared memory (SW128,
 //   K-major).  K and V of 128 local tokens per tile go through a 3-stage
-//   ring; the cache's pages are block_size tokens, so producer warps copy
-//   them with 16-byte cp.async into the SW128 layout (zeros past the rows'
-//   furthest position) and publish each stage after a proxy fence.
+//   ring.  When block_size is a multiple of 64, every 64 tokens of a tile lie
+//   in one page and come in as TMA boxes of [64 tokens x 64 columns] (SW128,
+//   8 boxes per tile, dealt over the producer warps); otherwise producer
+//   warps copy them with 16-byte cp.async into the same layout (zeros past
+//   the rows' furthest position) and publish each stage after a proxy fence.
+//   (Through TMA a tile's tokens past the shard's end come from the cache as
+//   stored; their probabilities are exactly 0, so they must hold finite
+//   values, as a zero-initialised pool does.)
 //   S = Q K^T (N = 128) lands in one of two TMEM buffers; the softmax warps
 //   (thread = row = TMEM lane) mask each row at its own bound, write P back
 //   as bf16 pairs over the buffer's first columns, and the P.V MMA reads it
@@ -24,6 +29,7 @@
 // TMEM: O [0, 128), S buffers [128, 256) and [256, 384).  Every wait is
 // bounded; a timeout raises DCP_DEV_ERR_TIMEOUT and the role stops.
 #include "dcp_internal.cuh"
+#include "mla_common.cuh"
 #include "sm100_prims.cuh"
 
 namespace dcp {
@@ -44,6 +50,7 @@ constexpr int kWarpMma = kProd;
 constexpr int kWarpSoftmax = kWarpMma + 1;
 constexpr int kThreads = 32 * (kWarpSoftmax + 4);
 constexpr float kRescaleLog2 = 8.f;
+constexpr int kMaxPages = 32;                // pages a tile may touch: kKeys / bs + 2 <= 32 needs bs >= 8
 
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kQBytes;
@@ -92,13 +99,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, int use_tma) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sQ = smem + kOffQ;
     uint8_t* sRing = smem + kOffRing;
     const Bars sh = carve(smem);
     __shared__ int s_kv;
+    __shared__ int32_t s_blk[kProd][32];  // block ids of the producers' current tile
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
@@ -126,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sh.full[i], kProdThreads);
+            mbar_init(&sh.full[i], use_tma ? 1 : kProdThreads);  // TMA: the expect-tx arrive; else every copier
             mbar_init(&sh.empty[i], 1);
         }
         mbar_init(sh.q_full, 128);
@@ -177,32 +187,92 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int kv = s_kv;
     const int ntiles = (kv + kKeys - 1) / kKeys;
 
-    if (warp < kProd) {
-        // ------------------------------------------------------------ producers
+    if (warp < kProd && use_tma) {
+        // ------------------------------------------------------------ TMA producers
+        // Box j of a tile (j = 4 kv + 2 g + h: K or V, token group g of 64,
+        // column half h) goes out from warp j % 3.  A group past the rows'
+        // furthest position re-reads group 0 (finite values, probability 0).
+        if (lane == 0) {
+            const int32_t* bt = a.block_tables + ((int64_t)r * a.B + b) * a.max_blocks;
+            bool alive = true, bad = false;
+            auto group_row = [&](int t, int g) -> int {  // first pool row of token group g of tile t
+                int lp0 = t * kKeys + 64 * g;
+                if (lp0 >= kv) lp0 = t * kKeys;
+                int32_t blk = bt[lp0 / a.bs];
+                if (blk < 0 || blk >= a.num_blocks) {
+                    bad = true;
+                    blk = 0;
+                }
+                return (int)(((int64_t)blk * a.Hkv + kvh) * a.bs + lp0 % a.bs);
+            };
+            int nrow0 = 0, nrow1 = 0;
+            if (ntiles > 0) { nrow0 = group_row(0, 0); nrow1 = group_row(0, 1); }
+            for (int t = 0; t < ntiles && alive; ++t) {
+                const int s = t % kStages;
+                const int row_g0 = nrow0, row_g1 = nrow1;
+                if (t + 1 < ntiles) { nrow0 = group_row(t + 1, 0); nrow1 = group_row(t + 1, 1); }
+                bool waited = false;
+                for (int j = warp; j < 8; j += kProd) {
+                    if (!waited) {
+                        if (!mbar_wait_sleep(&sh.empty[s], ((t / kStages) & 1) ^ 1u)) { alive = false; break; }
+                        waited = true;
+                    }
+                    if (j == 0) mbar_arrive_expect_tx(&sh.full[s], (uint32_t)kStageBytes);
+                    const int kvsel = j >> 2, g = (j >> 1) & 1, h = j & 1;
+                    uint8_t* dst = sRing + (size_t)s * kStageBytes + kvsel * 2 * kSub + h * kSub + g * 8192;
+                    if (kvsel)
+                        tma_load_2d(dst, &tmap_v, 64 * h, g ? row_g1 : row_g0, &sh.full[s]);
+                    else
+                        tma_load_2d(dst, &tmap_k, 64 * h, g ? row_g1 : row_g0, &sh.full[s]);
+                }
+            }
+            if (bad) raise_err(err, DCP_DEV_ERR_BLOCK_ID);
+            if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+        }
+    } else if (warp < kProd) {
+        // ------------------------------------------------------------ cp.async producers
+        // Thread pt copies the fixed 16-byte column c16 = pt % 16 of rows
+        // pt / 16 + 6 i of K and V.  A tile's block ids (at most kKeys / bs + 2
+        // pages) sit in a per-warp table, loaded one tile ahead so that no
+        // copy waits on a block-table read.
         const int pt = threadIdx.x;  // 0 .. 95
+        const int c16 = pt & 15, rbeg = pt >> 4;
+        constexpr int kRowStep = kProdThreads / 16;
         const int32_t* bt = a.block_tables + ((int64_t)r * a.B + b) * a.max_blocks;
-        const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k_pool);
-        const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v_pool);
+        const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k_pool) + c16 * 16;
+        const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v_pool) + c16 * 16;
         const uint32_t ring = smem_u32(sRing);
+        const bool pow2 = (a.bs & (a.bs - 1)) == 0;
+        const int bsh = __ffs(a.bs) - 1;
+        auto page_of = [&](int lp) -> int { return pow2 ? lp >> bsh : lp / a.bs; };
+        auto page_id = [&](int t) -> int32_t {  // this lane's page of tile t
+            const int pg = page_of(t * kKeys) + lane;
+            return (lane < kMaxPages && pg * a.bs < kv) ? bt[pg] : -1;
+        };
         bool alive = true, bad = false;
+        int32_t nxt = ntiles > 0 ? page_id(0) : -1;
         for (int t = 0; t < ntiles && alive; ++t) {
             const int s = t % kStages;
             if (lane == 0 && !mbar_wait_sleep(&sh.empty[s], ((t / kStages) & 1) ^ 1u)) alive = false;
             alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
             if (!alive) break;
+            s_blk[warp][lane] = nxt;
+            __syncwarp();
+            if (t + 1 < ntiles) nxt = page_id(t + 1);
+            const int pg0 = page_of(t * kKeys);
             const uint32_t st = ring + (uint32_t)s * kStageBytes;
-            for (int idx = pt; idx < kKeys * 16; idx += kProdThreads) {
-                const int row = idx >> 4, c16 = idx & 15;
+            for (int row = rbeg; row < kKeys; row += kRowStep) {
                 const int lp = t * kKeys + row;
                 bool valid = lp < kv;
                 int64_t off = 0;
                 if (valid) {
-                    const int32_t blk = bt[lp / a.bs];
+                    const int32_t blk = s_blk[warp][page_of(lp) - pg0];
                     if (blk < 0 || blk >= a.num_blocks) {
                         bad = true;
                         valid = false;
                     } else {
-                        off = ((((int64_t)blk * a.Hkv + kvh) * a.bs + lp % a.bs) * kD + c16 * 8) * 2;
+                        const int in_pg = pow2 ? (lp & (a.bs - 1)) : lp % a.bs;
+                        off = (((int64_t)blk * a.Hkv + kvh) * a.bs + in_pg) * (kD * 2);
                     }
                 }
                 const uint32_t so = sw128(row, c16);
@@ -210,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 cp_async16_zfill(st + 2 * kSub + so, vp + off, valid);
             }
             cp_async_commit();
+            __syncwarp();  // the table is rewritten for the next tile
             if (t > 0) {
                 cp_async_wait<1>();
                 fence_proxy_async_smem();
@@ -399,14 +470,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 }  // namespace
 
 bool prefill_tc_supported(const PrefillArgs& a) {
-    return a.D == kD && a.G >= 1 && kRows % a.G == 0;
+    return a.D == kD && a.G >= 1 && kRows % a.G == 0 && a.bs >= 8;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
+    CUtensorMap tk, tv;
+    memset(&tk, 0, sizeof tk);
+    memset(&tv, 0, sizeof tv);
+    const int use_tma = a.bs % 64 == 0 ? 1 : 0;
+    if (use_tma) {
+        // the pools as [num_blocks * Hkv * block_size rows x 128 columns], boxes of 64 x 64
+        const uint64_t rows = (uint64_t)a.num_blocks * a.Hkv * a.bs;
+        if (!mla::make_map_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k_pool, kD, rows, kD * 2, 64, 64,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !mla::make_map_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.v_pool, kD, rows, kD * 2, 64, 64,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
     const int64_t ctas = ((int64_t)a.Tq * a.G + kRows - 1) / kRows * ((int64_t)a.B * a.Hkv * a.N);
-    return launch_pdl(prefill_tc_kernel, dim3((unsigned)ctas), dim3(kThreads), kSmem, s, a);
+    return launch_pdl(prefill_tc_kernel, dim3((unsigned)ctas), dim3(kThreads), kSmem, s, a, tk, tv, use_tma);
 }
 
 }  // namespace dcp

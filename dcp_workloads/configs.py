@@ -51,11 +51,12 @@ CONFIGS = {
     # Prefill under PCP x DCP (the head-tail partition and causal prefill
     # path): a 2K-token chunk on top of a 64K cached context (the chunk and
     # context of the pages' prefill-overhead figure), Llama-8B-like GQA layer,
-    # 4 DCP ranks holding the KV, 4 PCP ranks splitting the chunk.  Tq is the
-    # chunk; every request's last Tq tokens are the new ones.
+    # 4 DCP ranks holding the KV, 4 PCP ranks splitting the chunk, 64-token
+    # pages (as the MLA configs).  Tq is the chunk; every request's last Tq
+    # tokens are the new ones.
     "gqa_prefill_64k": dict(
         index=6, layout="gqa", B=2, Tq=2048, Hq=32, Hkv=8, Dk=128, Dv=128,
-        lengths=("fixed", 64 * 1024 + 2048), N=4, I=1, block_size=16, pcp=4,
+        lengths=("fixed", 64 * 1024 + 2048), N=4, I=1, block_size=64, pcp=4,
         q_dtype="bf16", kv_dtype="bf16", out_dtype="bf16",
         softmax_scale=1.0 / math.sqrt(128),
     ),

@@ -26,6 +26,10 @@ CASES = {
     "d64_g2_n3_i5": (config("gqa_llama8b", B=2, Tq=40, Hq=8, Hkv=4, Dk=64, Dv=64, N=3, I=5,
                             lengths=("list", [333, 77])), 2),
     "whole_prompt_k3": (config("gqa_llama8b", B=1, Tq=300, lengths=("list", [300])), 3),
+    # block sizes that are multiples of 64: K/V come in through TMA boxes
+    "bs64_chunk192_k4": (config("gqa_llama8b", B=2, Tq=192, block_size=64, lengths=("list", [1000, 2600])), 4),
+    "bs128_chunk100_k2_N3": (config("gqa_llama8b", B=2, Tq=100, block_size=128, N=3, I=2,
+                                    lengths=("list", [100, 777])), 2),
 }
 
 _cache = {}
@@ -88,7 +92,7 @@ def test_prefill_merged_matches_oracle(name):
         assert np.all(got_o[pb, pj] == 0.0) and np.all(np.isneginf(got_l[pb, pj]))
 
 
-@pytest.mark.parametrize("name", ["llama8b_chunk256_k4", "llama8b_chunk64_k8_I16", "d64_g2_n3_i5"])
+@pytest.mark.parametrize("name", ["llama8b_chunk256_k4", "llama8b_chunk64_k8_I16", "d64_g2_n3_i5", "bs64_chunk192_k4"])
 def test_prefill_rank_partials_match_oracle(name):
     wl, dw, K = _setup(name)
     c = wl.cfg
