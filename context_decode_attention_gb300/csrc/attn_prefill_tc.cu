@@ -25,7 +25,11 @@
 //   O (128 x 128 fp32) stays in TMEM; the reference max is lazy (O is
 //   rescaled only when a row's max grows by more than 2^8).
 //
-// Warps: 0-2 producers, 3 TMEM owner and MMA issuer (one lane), 4-7 softmax.
+// Warps: 0-2 producers, 3 TMEM owner and MMA issuer (one lane), 4-7 and 8-11
+// softmax (two warpgroups over the same 128 rows, 64 columns of each tile
+// each: the exponentials of a tile are spread over twice the warps; the two
+// half-row maxima meet in shared memory, and each group writes P over its own
+// S columns and rescales / stores its own half of O).
 // TMEM: O [0, 128), S buffers [128, 256) and [256, 384).  Every wait is
 // bounded; a timeout raises DCP_DEV_ERR_TIMEOUT and the role stops.
 #include "dcp_internal.cuh"
@@ -48,7 +52,10 @@ constexpr int kProd = 3;                     // producer warps
 constexpr int kProdThreads = 32 * kProd;
 constexpr int kWarpMma = kProd;
 constexpr int kWarpSoftmax = kWarpMma + 1;
-constexpr int kThreads = 32 * (kWarpSoftmax + 4);
+constexpr int kSoftGroups = 2;              // softmax warpgroups, 64 of the tile's columns each
+constexpr int kGroupCols = kKeys / kSoftGroups;
+constexpr int kSoftThreads = 128 * kSoftGroups;
+constexpr int kThreads = 32 * kWarpSoftmax + kSoftThreads;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxPages = 32;                // pages a tile may touch: kKeys / bs + 2 <= 32 needs bs >= 8
 
@@ -109,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Bars sh = carve(smem);
     __shared__ int s_kv;
     __shared__ int32_t s_blk[kProd][32];  // block ids of the producers' current tile
+    __shared__ float s_xch[kSoftGroups][kRows];  // the softmax groups' half-row maxima, then row sums
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
@@ -139,10 +147,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.full[i], use_tma ? 1 : kProdThreads);  // TMA: the expect-tx arrive; else every copier
             mbar_init(&sh.empty[i], 1);
         }
-        mbar_init(sh.q_full, 128);
+        mbar_init(sh.q_full, kSoftThreads);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.s_full[i], 1);
-            mbar_init(&sh.p_full[i], 4);
+            mbar_init(&sh.p_full[i], 4 * kSoftGroups);
         }
         mbar_init(sh.o_done, 1);
         fence_mbar_init();
@@ -155,7 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();  // barriers initialised, s_kv zeroed
 
     // the softmax threads own the rows: position, causal bound, query row
-    const int h = threadIdx.x - 32 * kWarpSoftmax;  // row = TMEM lane (softmax warps)
+    const int hs = threadIdx.x - 32 * kWarpSoftmax;  // softmax thread
+    const int h = hs & (kRows - 1);                  // row = TMEM lane
+    const int grp = hs >> 7;                         // softmax group: columns [64 grp, 64 grp + 64)
     int t_row = 0;
     int32_t bound = 0;
     if (warp >= kWarpSoftmax) {
@@ -175,8 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  (((int64_t)b * a.Tq + t_row) * a.Hq + (int64_t)kvh * a.G + gq) * kD);
         }
 #pragma unroll
-        for (int c16 = 0; c16 < 16; ++c16)
+        for (int c = 0; c < 8; ++c) {
+            const int c16 = 8 * grp + c;  // each group stores half of the row
             *reinterpret_cast<uint4*>(sQ + sw128(h, c16)) = src ? src[c16] : make_uint4(0, 0, 0, 0);
+        }
         fence_proxy_async_smem();
         mbar_arrive(sh.q_full);
     }
@@ -313,8 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t pa = tm + 128 + 128 * sb;
                 const uint64_t vd = dvr + (uint64_t)(t % kStages) * kStageDesc;
 #pragma unroll 1
-                for (int kk = 0; kk < kKeys / 16; ++kk)
-                    mma_ts(tm, pa + 8 * kk, vd + 128 * kk, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kKeys / 16; ++kk)  // group g's P sits over columns [64 g, 64 g + 32)
+                    mma_ts(tm, pa + 8 * kk + (kk >= 4 ? 32 : 0), vd + 128 * kk, idesc_pv,
+                           (t > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&sh.empty[t % kStages]);
                 mma_commit(sh.o_done);
                 return true;
@@ -338,37 +351,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
         }
     } else {
-        // ------------------------------------------------------------ softmax warpgroup
+        // ------------------------------------------------------------ softmax warpgroups
         const int quarter = warp & 3;
         const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
         const float sl2 = a.softmax_scale * 1.4426950408889634f;
+        const int c0 = kGroupCols * grp;  // this group's columns of a tile
         float m_ref = -INFINITY, l = 0.f;
         bool alive = true;
-        // the tcgen05.ld / st below are warp-aligned: every wait's outcome is
-        // made uniform across the warp so that all lanes leave together
+        // barrier over the two groups that also ANDs a flag: both groups leave
+        // a loop together (a bar.sync cannot time out)
+        auto both = [&](int id, bool ok) -> bool {
+            uint32_t in = ok ? 1u : 0u, out;
+            asm volatile("{\n.reg .pred pi, po;\nsetp.ne.u32 pi, %1, 0;\nbar.red.and.pred po, %2, %3, pi;\n"
+                         "selp.u32 %0, 1, 0, po;\n}"
+                         : "=r"(out)
+                         : "r"(in), "r"(id), "r"(kSoftThreads)
+                         : "memory");
+            return out != 0;
+        };
         for (int t = 0; t < ntiles; ++t) {
             const int sb = t & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&sh.s_full[sb], (t >> 1) & 1))) { alive = false; break; }
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&sh.s_full[sb], (t >> 1) & 1));
             tc_fence_after();
-            const uint32_t sbase = tm + 128 + 128 * sb + lane_off;
-            // columns [0, lim) of this tile are visible to the row
-            const int lim = max(0, min(kKeys, bound - t * kKeys));
+            const uint32_t sbase = tm + 128 + 128 * sb + lane_off + c0;
+            // columns [0, lim) of this group's 64 are visible to the row
+            const int lim = max(0, min(kGroupCols, bound - t * kKeys - c0));
             float mraw = -INFINITY;
             {
                 uint32_t rr[32];
 #pragma unroll 1
-                for (int c = 0; c < kKeys / 32; ++c) {
+                for (int c = 0; c < kGroupCols / 32; ++c) {
                     tmem_ld32(sbase + 32 * c, rr);
                     tmem_wait_ld();
                     const int lc = lim - 32 * c;
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    if (lc >= 32) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        m4[k & 3] = fmaxf(m4[k & 3], (k < lc) ? __uint_as_float(rr[k]) : -INFINITY);
+                        for (int k = 0; k < 32; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(rr[k]));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            m4[k & 3] = fmaxf(m4[k & 3], (k < lc) ? __uint_as_float(rr[k]) : -INFINITY);
+                    }
                     mraw = fmaxf(mraw, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
                 }
             }
-            const float mx = (lim > 0) ? mraw * sl2 : -INFINITY;
+            s_xch[grp][h] = (lim > 0) ? mraw * sl2 : -INFINITY;
+            if (!both(1, ok)) { alive = false; break; }
+            const float mx = fmaxf(s_xch[0][h], s_xch[1][h]);  // the row's max over the tile (base 2)
+            // lazy reference max (both groups take the same decision)
             float corr = 1.f;
             bool rescale_o = false;
             if (mx > -INFINITY) {
@@ -382,9 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            // P as bf16 pairs over the group's first 32 columns (already read)
             float lsum = 0.f;
 #pragma unroll 1
-            for (int q = 0; q < kKeys / 16; ++q) {
+            for (int q = 0; q < kGroupCols / 16; ++q) {
                 uint32_t r16[16], pk[8];
                 tmem_ld16(sbase + 16 * q, r16);
                 tmem_wait_ld();
@@ -403,21 +435,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st8(sbase + 8 * q, pk);
             }
             l = (corr == 0.f ? 0.f : l * corr) + lsum;
-            // P.V of the previous tile must be complete before O is touched
-            if (t > 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(sh.o_done, (t - 1) & 1))) { alive = false; break; }
-                tc_fence_after();
-            }
+            // P.V of the previous tile must be complete before O is touched;
+            // the second barrier also keeps s_xch from being overwritten early
+            bool ok2 = true;
+            if (t > 0) ok2 = __all_sync(0xffffffffu, mbar_wait(sh.o_done, (t - 1) & 1));
+            if (!both(2, ok2)) { alive = false; break; }
+            tc_fence_after();
             if (__any_sync(0xffffffffu, rescale_o)) {
                 const float f = rescale_o ? corr : 1.f;
                 uint32_t ov[32];
 #pragma unroll 1
-                for (int i = 0; i < kD / 32; ++i) {
-                    tmem_ld32(tm + lane_off + 32 * i, ov);
+                for (int i = 0; i < kGroupCols / 32; ++i) {
+                    tmem_ld32(tm + lane_off + c0 + 32 * i, ov);
                     tmem_wait_ld();
 #pragma unroll
                     for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * f);
-                    tmem_st32(tm + lane_off + 32 * i, ov);
+                    tmem_st32(tm + lane_off + c0 + 32 * i, ov);
                 }
             }
             tmem_wait_st();
@@ -425,28 +458,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.p_full[sb]);
         }
-        // epilogue: the last P.V, then the row's normalised partial and LSE
-        if (alive && ntiles > 0) {
-            if (!__all_sync(0xffffffffu, mbar_wait(sh.o_done, (ntiles - 1) & 1))) alive = false;
-            tc_fence_after();
-        }
+        // epilogue: the last P.V, the row's total sum, then this group's half of
+        // the row's normalised partial (and, group 0, the LSE)
+        bool ok3 = alive;
+        if (alive && ntiles > 0) ok3 = __all_sync(0xffffffffu, mbar_wait(sh.o_done, (ntiles - 1) & 1));
+        s_xch[grp][h] = l;
+        const bool read_o = both(1, ok3) && ntiles > 0;  // uniform across both groups
+        tc_fence_after();
+        const float lt = s_xch[0][h] + s_xch[1][h];
         // every lane reads its TMEM lane (rows past the request too: the load
         // is warp-aligned); only the request's rows are written
         const bool row_ok = t_row < a.Tq;
-        const bool read_o = alive && ntiles > 0;  // uniform across the warp
-        const bool has = read_o && l > 0.f;
-        const float inv = has ? 1.f / l : 0.f;
+        const bool has = read_o && lt > 0.f;
+        const float inv = has ? 1.f / lt : 0.f;
         int64_t prow = 0;
         if (row_ok) {
             const int gq = (row0 + h) % a.G;
             prow = (((int64_t)r * a.B + b) * a.Tq + t_row) * a.Hq + (int64_t)kvh * a.G + gq;
         }
-        float* dst = a.out_partial + prow * kD;
+        float* dst = a.out_partial + prow * kD + c0;
         uint32_t ov[32];
 #pragma unroll 1
-        for (int i = 0; i < kD / 32; ++i) {
+        for (int i = 0; i < kGroupCols / 32; ++i) {
             if (read_o) {
-                tmem_ld32(tm + lane_off + 32 * i, ov);
+                tmem_ld32(tm + lane_off + c0 + 32 * i, ov);
                 tmem_wait_ld();
             }
             if (row_ok) {
@@ -458,8 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        if (row_ok) a.lse_partial[prow] = has ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
-        if (!alive && lane == 0) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+        if (row_ok && grp == 0) a.lse_partial[prow] = has ? (m_ref + log2f(lt)) * 0.6931471805599453f : -INFINITY;
+        if (!read_o && ntiles > 0 && lane == 0) raise_err(err, DCP_DEV_ERR_TIMEOUT);
     }
     tc_fence_before();
     __syncthreads();
