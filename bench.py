@@ -58,8 +58,8 @@ MEASURED_TRAFFIC = {
     ("transfer_blocks", "entry"): ("transfer.cu", "ba69fc5af5bf509387a4668d62e0fd322f75cc04daf9e1105750d478aee93893",
                                    (161.792e3 + 0.0) / (8 * 16 * 284)),
     # per request of the prefill workload's shape (2K chunk on a 64K context)
-    ("prefill", "request"): ("attn_prefill.cu", "26cd0da72bfc457f818172126161555cdabf17b9b5d19fe389ad783d0b8d8d95",
-                             295.139584e6 + 115.376896e6),
+    ("prefill", "request"): ("attn_prefill_tc.cu", "8608f7c006c096a93a90bbcbcbf098974209e440eb6f9480f60e124e04491360",
+                             294.589440e6 + 112.330240e6),
 }
 
 
@@ -495,8 +495,8 @@ def run_prefill(args):
             "traffic": measured_traffic("prefill", "request", B) if name == "gqa_prefill_64k" and not args.context else None,
             "traffic_note": "ncu DRAM bytes of one request's launch (profiles/), times the requests",
             "algorithmic_flops": flops,
-            "peak_source": peaks["source"] + " (MEASURED_PEAKS.json, burst; bf16 operands on mma.sync)",
-            "kernel": "prefill_partial_kernel", "attn_ms": attn_ms,
+            "peak_source": peaks["source"] + " (MEASURED_PEAKS.json, burst; bf16 tcgen05 kind::f16)",
+            "kernel": "prefill_tc_kernel" if int(cfg["Dk"]) == 128 else "prefill_partial_kernel", "attn_ms": attn_ms,
             "roofline_ms": 1e3 * flops / (peaks["bf16_tflops"] * 1e12)}
     line = {
         "metric": PREFILL_METRIC, "value": world * B * Tq / (step_ms / 1e3), "unit": "tokens/s", "n_gpus": world,
