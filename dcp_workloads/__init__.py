@@ -3,12 +3,13 @@
 This module is shared by the CUDA path's tests/bench and by the oracle's tests.
 It holds no arithmetic of the method itself: it only draws random numbers,
 rounds them to the storage dtype with library casts, lays tokens out densely
-per request, and hands out physical block ids from a random permutation once a
-caller has said how many blocks each (rank, request) needs.
+per request, hands out physical block ids from a random permutation once a
+caller has said how many blocks each (rank, request) needs, and draws the
+candidate positions a sparse-attention indexer would select.
 """
 
 from .configs import CONFIGS, CONFIG_ORDER, config
-from .gen import Workload, make_workload, allocate_blocks, bf16_bits, fp8_bits
+from .gen import Workload, make_workload, allocate_blocks, bf16_bits, fp8_bits, sparse_candidates
 
 __all__ = [
     "CONFIGS",
@@ -19,4 +20,5 @@ __all__ = [
     "allocate_blocks",
     "bf16_bits",
     "fp8_bits",
+    "sparse_candidates",
 ]

@@ -211,3 +211,20 @@ def allocate_blocks(rank_blocks: np.ndarray, seed: int, spare: int = 0):
             tables[r, b, :n] = perm[pos:pos + n]
             pos += n
     return tables, num_blocks
+
+
+def sparse_candidates(wl: Workload, k: int, seed: int = 0) -> np.ndarray:
+    """A synthetic top-k indexer: for every query token (b, t) -- position
+    L_b - Tq + t -- k distinct positions drawn uniformly from the ones it may
+    attend to (0 .. its own position), sorted ascending; all of them when
+    fewer are visible, -1 after the last.  Returns int32 [B * Tq, k]."""
+    Tq = int(wl.cfg["Tq"])
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(wl.seed), int(seed), 0x70C])))
+    out = np.full((wl.B * Tq, k), -1, dtype=np.int32)
+    for b in range(wl.B):
+        L = int(wl.seq_lens[b])
+        for t in range(Tq):
+            vis = L - Tq + t + 1
+            pick = np.arange(vis) if vis <= k else np.sort(rng.choice(vis, size=k, replace=False))
+            out[b * Tq + t, :len(pick)] = pick
+    return out

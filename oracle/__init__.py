@@ -14,6 +14,8 @@ Functions (all numpy in, numpy out):
   pcp_partition(K, ctx_lens, q_lens, max_q)  head-tail prefill partition
   attention(wl, rank=-1, rows=None)      (out [rows, Dv], lse [rows]) in fp64
   merge(o_parts, lse_parts)              exact LSE merge of per-rank partials
+  sparse_localize(cand, N, I, seq_lens, Tq)  per-rank local positions of candidates
+  sparse_attention(wl, cand, rank=-1)    attention over each query's candidate set
   decode(raw, dtype, scale)              stored values -> float64
 
 Every function follows one passage of the pages; the C source's header lists
@@ -176,3 +178,75 @@ def merge(o_parts, lse_parts):
     lse = np.empty(max(1, rows), dtype=np.float64)
     _load().orc_merge(N, rows, Dv, _ptr(o_parts), _ptr(lse_parts), _ptr(out), _ptr(lse))
     return out[:rows], lse[:rows]
+
+
+def sparse_localize(cand, N, I, seq_lens, Tq):
+    """Candidate localization under DCP ("vLLM DCP and PCP", the indexer
+    localisation tests in its source-and-test table; "GLM-5.3 ... Part 2":
+    sparse MLA attends to a selected token set).  For every query row's
+    candidate list (global positions, -1 unused), each rank's candidates in
+    list order, as its local positions (ownership by the rank equation, local
+    positions by the running count of local_layout).  Returns (local [N, rows,
+    k] int32 padded with -1, counts [N, rows] int32)."""
+    cand = np.asarray(cand, dtype=np.int64)
+    rows, k = cand.shape
+    local = np.full((N, rows, k), -1, dtype=np.int32)
+    counts = np.zeros((N, rows), dtype=np.int32)
+    layouts = {}
+    for i in range(rows):
+        b = i // Tq
+        L = int(seq_lens[b])
+        if L not in layouts:
+            layouts[L] = local_layout(L, N, I)
+        rk, lp = layouts[L]
+        for t in cand[i]:
+            if t < 0:
+                continue
+            r = int(rk[t])
+            local[r, i, counts[r, i]] = lp[t]
+            counts[r, i] += 1
+    return local, counts
+
+
+def sparse_attention(wl, cand, rank=-1, N=None, I=None):
+    """Attention of every query token's heads over its candidate set only, in
+    fp64: s_j = scale * q . k_j over the candidates, o = softmax(s) V,
+    L = logsumexp(s).  rank >= 0 keeps the candidates that rank owns (a
+    rank's partial; empty: zeros and -inf).  Returns (out [rows*Hq, Dv],
+    lse [rows*Hq]) with rows = B * Tq, row order (b, t, h)."""
+    c = wl.cfg
+    B, Tq, Hq, Hkv, Dk, Dv = (int(c[x]) for x in ("B", "Tq", "Hq", "Hkv", "Dk", "Dv"))
+    N = int(c["N"]) if N is None else N
+    I = int(c["I"]) if I is None else I
+    G = Hq // Hkv
+    mla = c["layout"] == "mla"
+    scale = float(c["softmax_scale"])
+    cand = np.asarray(cand, dtype=np.int64)
+    out = np.zeros((B * Tq * Hq, Dv))
+    lse = np.full(B * Tq * Hq, -np.inf)
+    layouts = {}
+    for b in range(B):
+        L = int(wl.seq_lens[b])
+        if rank >= 0 and L not in layouts:
+            layouts[L] = local_layout(L, N, I)
+        for t in range(Tq):
+            i = b * Tq + t
+            C = cand[i][cand[i] >= 0]
+            if rank >= 0:
+                C = C[layouts[L][0][C] == rank]
+            if C.size == 0:
+                continue
+            rows_kv = wl.req_start[b] + C
+            q = decode(wl.q[b, t], c["q_dtype"])                      # [Hq, Dk]
+            kk = decode(wl.k[rows_kv], c["kv_dtype"], wl.kv_scale)    # [n, Hkv, Dk]
+            vv = kk[:, :, :Dv] if mla else decode(wl.v[rows_kv], c["kv_dtype"], wl.kv_scale)
+            for h in range(Hq):
+                g = h // G
+                s = scale * (kk[:, g, :] @ q[h])
+                m = s.max()
+                w = np.exp(s - m)
+                l = w.sum()
+                r = (i * Hq) + h
+                lse[r] = m + np.log(l)
+                out[r] = (w @ vv[:, g, :]) / l
+    return out, lse

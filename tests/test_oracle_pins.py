@@ -450,3 +450,75 @@ def test_pcp_partition_padding_and_overflow():
     assert r["pos"][2].tolist()[:4] == [5, 8, 6, 7]
     bad = oracle.pcp_partition(4, [0], [9], 8)   # aligned to 16 > 8 rows
     assert bad["status"] == -1 and (bad["pos"] == -1).all()
+
+
+# ------------------------------------------------ sparse (top-k) attention
+
+from dcp_workloads import sparse_candidates  # noqa: E402
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("mla_fp8_mixed", dict(B=2, lengths=("list", [40, 90]))),
+    ("gqa_llama8b", dict(B=2, Tq=3, lengths=("list", [30, 70]))),
+])
+def test_sparse_with_every_position_is_dense(name, kw):
+    """A candidate set holding every visible position reduces to the pinned
+    dense (causal) attention."""
+    wl = make_workload(config(name, **kw), seed=4)
+    cand = sparse_candidates(wl, 4096)            # k above every length: all visible positions
+    so, sl = oracle.sparse_attention(wl, cand)
+    do, dl = oracle.attention(wl)
+    assert np.allclose(so, do, atol=1e-12, rtol=0) and np.allclose(sl, dl, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("N,I", [(2, 1), (8, 1), (4, 64), (3, 5)])
+def test_sparse_rank_partials_merge_to_sparse(N, I):
+    wl = make_workload(config("mla_fp8_mixed", B=2, N=N, I=I, lengths=("list", [700, 1500])), seed=5)
+    cand = sparse_candidates(wl, 200)
+    full_o, full_l = oracle.sparse_attention(wl, cand)
+    parts = [oracle.sparse_attention(wl, cand, rank=r) for r in range(N)]
+    mo, ml = oracle.merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    assert np.allclose(mo, full_o, atol=1e-12, rtol=0) and np.allclose(ml, full_l, atol=1e-12, rtol=0)
+
+
+def test_sparse_single_candidate_and_order():
+    wl = make_workload(config("gqa_llama8b", B=1, lengths=("list", [50])), seed=6)
+    c = wl.cfg
+    cand = np.full((1, 4), -1, dtype=np.int32)
+    cand[0, 0] = 17
+    o, l = oracle.sparse_attention(wl, cand)
+    q = oracle.decode(wl.q[0, 0], "bf16")
+    k = oracle.decode(wl.k[17], "bf16")
+    v = oracle.decode(wl.v[17], "bf16")
+    G = int(c["Hq"]) // int(c["Hkv"])
+    for h in range(int(c["Hq"])):
+        assert np.allclose(o[h], v[h // G], atol=1e-12)
+        assert abs(l[h] - float(c["softmax_scale"]) * float(q[h] @ k[h // G])) < 1e-12
+    # the candidate order does not matter
+    base = sparse_candidates(wl, 20)
+    shuffled = base.copy()
+    np.random.default_rng(0).shuffle(shuffled[0, :20])
+    a, la = oracle.sparse_attention(wl, base)
+    b, lb = oracle.sparse_attention(wl, shuffled)
+    assert np.allclose(a, b, atol=1e-12) and np.allclose(la, lb, atol=1e-12)
+
+
+@pytest.mark.parametrize("N,I", [(8, 1), (4, 16), (3, 5)])
+def test_sparse_localize_matches_closed_form(N, I):
+    """Per rank, the candidates it owns in list order, at their local
+    positions; checked against the closed form floor(t / (N I)) I + t mod I
+    (the oracle uses the running-count definition)."""
+    seq_lens = np.array([1000, 37], dtype=np.int32)
+    rng = np.random.default_rng(1)
+    cand = np.full((2, 64), -1, dtype=np.int32)
+    for i, L in enumerate(seq_lens):
+        n = min(64, int(L))
+        cand[i, :n] = rng.choice(int(L), size=n, replace=False)
+    local, counts = oracle.sparse_localize(cand, N, I, seq_lens, 1)
+    for i in range(2):
+        c = cand[i][cand[i] >= 0].astype(np.int64)
+        assert int(counts[:, i].sum()) == c.size
+        for r in range(N):
+            mine = c[(c // I) % N == r]
+            assert np.array_equal(local[r, i, :counts[r, i]], (mine // (N * I)) * I + mine % I)
+            assert np.all(local[r, i, counts[r, i]:] == -1)
