@@ -7,6 +7,7 @@ back to the CPU: if the library is missing or cannot load, every call raises.
 
 Functions carry the C ABI's names (include/dcp.h):
   dcp_workspace_size, dcp_workspace_init, dcp_get_error, dcp_slot_mapping, dcp_transfer_blocks, dcp_pcp_partition, dcp_prefill_attention,
+  dcp_sparse_workspace_size, dcp_sparse_localize, dcp_sparse_decode_attention,
   dcp_partial_attention, dcp_lse_merge, dcp_decode_attention
 """
 
@@ -21,7 +22,7 @@ from ._lib import (
 __all__ = [
     "DcpError", "DcpParams", "params_from_config", "lib", "lib_path",
     "dcp_workspace_size", "dcp_workspace_init", "dcp_get_error", "dcp_slot_mapping", "dcp_transfer_blocks", "dcp_pcp_partition",
-    "dcp_prefill_attention",
+    "dcp_prefill_attention", "dcp_sparse_workspace_size", "dcp_sparse_localize", "dcp_sparse_decode_attention",
     "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention", "dcp_decode_attention_noalloc",
     "dcp_launch_count",
     "dcp_attention_kernel", "DCP_F32", "DCP_BF16", "DCP_FP8_E4M3", "DCP_LAYOUT_GQA", "DCP_LAYOUT_MLA",
@@ -133,6 +134,30 @@ def dcp_prefill_attention(params, q, q_pos, k_pool, v_pool, num_blocks, block_ta
                                        int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(local_lens),
                                        _ptr(out_partial), _ptr(lse_partial), _ptr(out), _ptr(lse), _ptr(workspace),
                                        _nbytes(workspace), _stream(stream)), "dcp_prefill_attention")
+
+
+def dcp_sparse_workspace_size(params, B, k):
+    n = ctypes.c_size_t(0)
+    _check(lib().dcp_sparse_workspace_size(ctypes.byref(params), int(B), int(k), ctypes.byref(n)),
+           "dcp_sparse_workspace_size")
+    return int(n.value)
+
+
+def dcp_sparse_localize(params, cand, seq_lens, local, counts, workspace=None, stream=None):
+    """Each rank's candidates (cand [B*Tq, k]) at their local positions; see include/dcp.h."""
+    _check(lib().dcp_sparse_localize(ctypes.byref(params), int(seq_lens.numel()), int(cand.shape[-1]), _ptr(cand),
+                                     _ptr(seq_lens), _ptr(local), _ptr(counts), _ptr(workspace), _nbytes(workspace),
+                                     _stream(stream)), "dcp_sparse_localize")
+
+
+def dcp_sparse_decode_attention(params, q, cand, k_pool, num_blocks, block_tables, seq_lens, out, lse=None,
+                                workspace=None, stream=None):
+    """Attention of every query row over its candidate positions only, DCP-localised; see include/dcp.h."""
+    _check(lib().dcp_sparse_decode_attention(ctypes.byref(params), int(q.shape[0]), int(cand.shape[-1]), _ptr(q),
+                                             _ptr(cand), _ptr(k_pool), int(num_blocks), _ptr(block_tables),
+                                             int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(out), _ptr(lse),
+                                             _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "dcp_sparse_decode_attention")
 
 
 def dcp_partial_attention(params, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens,

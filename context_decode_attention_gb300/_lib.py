@@ -12,7 +12,8 @@ DCP_LAYOUT_GQA, DCP_LAYOUT_MLA = 0, 1
 # every symbol include/dcp.h declares
 EXPORTS = [
     "dcp_version", "dcp_error_string", "dcp_launch_count", "dcp_attention_kernel", "dcp_workspace_size", "dcp_workspace_init", "dcp_get_error",
-    "dcp_slot_mapping", "dcp_transfer_blocks", "dcp_pcp_partition", "dcp_prefill_attention", "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention",
+    "dcp_slot_mapping", "dcp_transfer_blocks", "dcp_pcp_partition", "dcp_prefill_attention",
+    "dcp_sparse_workspace_size", "dcp_sparse_localize", "dcp_sparse_decode_attention", "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention",
     "dcp_decode_attention_noalloc",
 ]
 
@@ -63,6 +64,9 @@ def lib():
         "dcp_slot_mapping": (ctypes.c_int, [P, i32, p, i64, p, p, p, i32, i64, p, p, p, p, p, p, p, p, p, p, sz, p]),
         "dcp_transfer_blocks": (ctypes.c_int, [P, i32, p, p, i32, i64, p, p, p, p, p, sz, p]),
         "dcp_pcp_partition": (ctypes.c_int, [i32, i32, p, p, i32, p, p, p, sz, p]),
+        "dcp_sparse_workspace_size": (ctypes.c_int, [P, i32, i32, ctypes.POINTER(sz)]),
+        "dcp_sparse_localize": (ctypes.c_int, [P, i32, i32, p, p, p, p, p, sz, p]),
+        "dcp_sparse_decode_attention": (ctypes.c_int, [P, i32, i32, p, p, p, i64, p, i32, p, p, p, p, sz, p]),
         "dcp_prefill_attention": (ctypes.c_int, [P, i32, i32, p, p, p, p, i64, p, i32, p, p, p, p, p, p, p, sz, p]),
         "dcp_partial_attention": (ctypes.c_int, [P, i32, p, p, p, i64, p, i32, p, p, p, p, p, sz, p]),
         "dcp_lse_merge": (ctypes.c_int, [i32, i64, i32, p, p, p, i32, p, p]),

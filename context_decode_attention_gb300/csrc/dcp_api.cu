@@ -106,7 +106,7 @@ int run_attention(const dcp_params* params, int32_t B, const void* q, const void
                   const void* v_pool, int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks,
                   const int32_t* seq_lens, const int32_t* local_lens, bool partial_mode, float* out_partial,
                   float* lse_partial, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, bool empty_ok = false) {
     int rc = validate_params(params);
     if (rc != DCP_OK) return rc;
     const dcp_params& p = *params;
@@ -142,7 +142,7 @@ int run_attention(const dcp_params* params, int32_t B, const void* q, const void
     PlanArgs pa;
     memset(&pa, 0, sizeof pa);
     pa.N = p.N; pa.I = p.I; pa.bs = p.block_size; pa.Hkv = p.Hkv; pa.Tq = p.Tq; pa.CH = a.CH; pa.B = B;
-    pa.partial_mode = a.partial_mode; pa.W = W; pa.max_blocks = max_blocks; pa.seq_lens = seq_lens;
+    pa.partial_mode = a.partial_mode; pa.W = W; pa.empty_ok = empty_ok ? 1 : 0; pa.max_blocks = max_blocks; pa.seq_lens = seq_lens;
     pa.local_lens = local_lens; pa.ws = a.ws; pa.lay = lay; pa.U = a.U; pa.G = a.Gn;
     pa.rows_per_group = a.rows; pa.Hq = p.Hq; pa.Dv = p.Dv; pa.out_partial = out_partial;
     pa.lse_partial = lse_partial; pa.out = out; pa.lse = lse; pa.out_dtype = p.out_dtype;
@@ -170,6 +170,52 @@ int run_attention(const dcp_params* params, int32_t B, const void* q, const void
         }
     }
     return e == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
+// ---- DCP-localised sparse attention ------------------------------------------
+// Workspace: the dense pass's own workspace first (its header is the caller's
+// error word), then the localised lists, the staging cache and the partials.
+struct SparseLayout {
+    size_t inner, local, counts, st_q, st_pool, st_tables, st_lens, part_o, part_lse, total;
+    int64_t R, S;
+    int kpad;
+};
+
+bool sparse_layout(const dcp_params& p, int32_t B, int32_t k, dcp_params* inner, SparseLayout* L) {
+    *inner = p;
+    inner->N = 1;
+    inner->I = 1;
+    inner->block_size = 64;
+    inner->Tq = 1;
+    L->R = (int64_t)B * p.Tq;
+    L->S = L->R * p.N;
+    L->kpad = (k + 63) / 64 * 64;
+    WsLayout lay;
+    Kernel kern;
+    int64_t W;
+    if (!layout_for(*inner, (int32_t)L->S, &lay, &kern, &W)) return false;
+    const size_t esz = p.kv_dtype == DCP_FP8_E4M3 ? 1 : (p.kv_dtype == DCP_BF16 ? 2 : 4);
+    size_t o = align256(lay.total);
+    L->inner = lay.total;
+    L->local = o; o = align256(o + sizeof(int32_t) * (size_t)(p.N * L->R * k));
+    L->counts = o; o = align256(o + sizeof(int32_t) * (size_t)(p.N * L->R));
+    L->st_q = o; o = align256(o + (size_t)L->S * p.Hq * p.Dk * 2);
+    L->st_pool = o; o = align256(o + (size_t)L->S * L->kpad * p.Dk * esz);
+    L->st_tables = o; o = align256(o + sizeof(int32_t) * (size_t)(L->S * (L->kpad / 64)));
+    L->st_lens = o; o = align256(o + sizeof(int32_t) * (size_t)L->S);
+    L->part_o = o; o = align256(o + sizeof(float) * (size_t)L->S * p.Hq * p.Dv);
+    L->part_lse = o; o = align256(o + sizeof(float) * (size_t)L->S * p.Hq);
+    L->total = o;
+    return true;
+}
+
+int sparse_check(const dcp_params* params, int32_t B, int32_t k) {
+    int rc = validate_params(params);
+    if (rc != DCP_OK) return rc;
+    const dcp_params& p = *params;
+    if (p.layout != DCP_LAYOUT_MLA || p.q_dtype != DCP_BF16 || p.N > 32) return DCP_ERR_UNSUPPORTED;
+    if (B < 0 || k < 1) return DCP_ERR_INVALID_ARG;
+    return DCP_OK;
 }
 
 }  // namespace
@@ -326,6 +372,82 @@ int dcp_prefill_attention(const dcp_params* params, int32_t B, int32_t Tq, const
             return DCP_ERR_CUDA;
     }
     return DCP_OK;
+}
+
+
+int dcp_sparse_workspace_size(const dcp_params* params, int32_t B, int32_t k, size_t* bytes) {
+    int rc = sparse_check(params, B, k);
+    if (rc != DCP_OK) return rc;
+    if (!bytes) return DCP_ERR_INVALID_ARG;
+    dcp_params inner;
+    SparseLayout L;
+    if (!sparse_layout(*params, B, k, &inner, &L)) return DCP_ERR_CUDA;
+    *bytes = L.total;
+    return DCP_OK;
+}
+
+int dcp_sparse_localize(const dcp_params* params, int32_t B, int32_t k, const int32_t* cand, const int32_t* seq_lens,
+                        int32_t* local, int32_t* counts, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+    int rc = sparse_check(params, B, k);
+    if (rc != DCP_OK) return rc;
+    if (!workspace || workspace_bytes < 256) return DCP_ERR_WORKSPACE;
+    if (B == 0) return DCP_OK;
+    if (!cand || !seq_lens || !local || !counts) return DCP_ERR_INVALID_ARG;
+    const dcp_params& p = *params;
+    return launch_sparse_localize(p.N, p.I, B * p.Tq, p.Tq, k, cand, seq_lens, local, counts,
+                                  &reinterpret_cast<WsHeader*>(workspace)->err, stream) == cudaSuccess
+               ? DCP_OK
+               : DCP_ERR_CUDA;
+}
+
+int dcp_sparse_decode_attention(const dcp_params* params, int32_t B, int32_t k, const void* q, const int32_t* cand,
+                                const void* k_pool, int64_t num_blocks, const int32_t* block_tables,
+                                int32_t max_blocks, const int32_t* seq_lens, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+    int rc = sparse_check(params, B, k);
+    if (rc != DCP_OK) return rc;
+    if (B == 0) return DCP_OK;
+    if (!q || !cand || !k_pool || !block_tables || !seq_lens || !out) return DCP_ERR_INVALID_ARG;
+    if (num_blocks < 1 || max_blocks < 1 || !aligned16(q) || !aligned16(k_pool)) return DCP_ERR_INVALID_ARG;
+    if (!workspace) return DCP_ERR_WORKSPACE;
+    const dcp_params& p = *params;
+    dcp_params inner;
+    SparseLayout L;
+    if (!sparse_layout(p, B, k, &inner, &L)) return DCP_ERR_CUDA;
+    if (workspace_bytes < L.total) return DCP_ERR_WORKSPACE;
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    int32_t* local = reinterpret_cast<int32_t*>(ws + L.local);
+    int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+    uint32_t* err = &reinterpret_cast<WsHeader*>(ws)->err;
+    // 1. each rank's candidates at their local positions
+    if (launch_sparse_localize(p.N, p.I, (int)L.R, p.Tq, k, cand, seq_lens, local, counts, err, stream) !=
+        cudaSuccess)
+        return DCP_ERR_CUDA;
+    // 2. staging: request r R + i holds rank r's candidate rows of query row i
+    SparseStageArgs sa;
+    memset(&sa, 0, sizeof sa);
+    sa.N = p.N; sa.R = (int)L.R; sa.Tq = p.Tq; sa.B = B; sa.k = k; sa.kpad = L.kpad; sa.bs = p.block_size;
+    sa.max_blocks = max_blocks; sa.num_blocks = num_blocks;
+    sa.row_bytes = p.Dk * (p.kv_dtype == DCP_FP8_E4M3 ? 1 : (p.kv_dtype == DCP_BF16 ? 2 : 4));
+    sa.q_row_bytes = p.Hq * p.Dk * 2;
+    sa.local = local; sa.counts = counts; sa.block_tables = block_tables; sa.k_pool = k_pool; sa.q = q;
+    sa.st_pool = ws + L.st_pool; sa.st_q = ws + L.st_q;
+    sa.st_tables = reinterpret_cast<int32_t*>(ws + L.st_tables);
+    sa.st_lens = reinterpret_cast<int32_t*>(ws + L.st_lens);
+    sa.err = err;
+    if (launch_sparse_stage(sa, stream) != cudaSuccess) return DCP_ERR_CUDA;
+    // 3. the rank partials: dense decode partials with one virtual rank
+    float* part_o = reinterpret_cast<float*>(ws + L.part_o);
+    float* part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+    rc = run_attention(&inner, (int32_t)L.S, sa.st_q, sa.st_pool, nullptr, L.S * (L.kpad / 64), sa.st_tables,
+                       L.kpad / 64, sa.st_lens, sa.st_lens, true, part_o, part_lse, nullptr, nullptr, workspace,
+                       L.inner, stream, /*empty_ok=*/true);
+    if (rc != DCP_OK) return rc;
+    // 4. exact LSE merge over the ranks
+    return launch_lse_merge(p.N, L.R * p.Hq, p.Dv, part_o, part_lse, out, p.out_dtype, lse, stream) == cudaSuccess
+               ? DCP_OK
+               : DCP_ERR_CUDA;
 }
 
 int dcp_partial_attention(const dcp_params* params, int32_t B, const void* q, const void* k_pool,

@@ -254,6 +254,46 @@ int dcp_prefill_attention(const dcp_params* params, int32_t B, int32_t Tq, const
                           size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * DCP-localised sparse (top-k) attention, MLA layout ("GLM-5.3 Optimizations,
+ * Part 2": sparse MLA attends to a selected set of 2,048 tokens per query,
+ * chosen by an indexer; "vLLM DCP and PCP", its source-and-test table: under
+ * DCP the candidates are localised to the ranks that own them, and the exact
+ * result is the LSE merge of the ranks' partials).
+ *
+ * Query row i = b * Tq + t (params->Tq query tokens per request, at
+ * positions seq_lens[b] - Tq + t) attends to the candidate positions
+ * cand[i][0..k) (device int32, global positions of request b, -1 = unused;
+ * a candidate past the row's own position raises DCP_DEV_ERR_TOKEN and is
+ * dropped).  N <= 32.
+ *
+ * dcp_sparse_localize: for every rank r and row i, rank r's candidates in
+ * list order at their local positions: local[r][i][0..counts[r][i]) (device
+ * int32 [N][B Tq][k], -1 after the last) and counts[r][i] (device int32
+ * [N][B Tq]).  workspace: its error word (>= 256 bytes).
+ *
+ * dcp_sparse_decode_attention: out[i][h][:] (params' out dtype) and lse[i][h]
+ * (optional, fp32) = attention of row i's heads over its candidates only.
+ * Localises the candidates, stages every (rank, row) candidate list as a
+ * contiguous 64-token-paged sequence in the workspace, computes the rank
+ * partials with the dense decode kernels (one virtual rank each) and merges
+ * them.  q [B][Tq][Hq][Dk] bf16; k_pool / block tables / seq_lens as for
+ * dcp_decode_attention (MLA: one latent row per token, no v_pool).  A row
+ * with no candidate gets zeros and -inf.  workspace: at least
+ * dcp_sparse_workspace_size bytes, zeroed once by dcp_workspace_init
+ * (includes a staging cache sized for every rank holding all k candidates of
+ * every row).  Non-MLA layouts or non-bf16 queries: DCP_ERR_UNSUPPORTED.
+ * Asynchronous on `stream`.
+ */
+int dcp_sparse_workspace_size(const dcp_params* params, int32_t B, int32_t k, size_t* bytes);
+int dcp_sparse_localize(const dcp_params* params, int32_t B, int32_t k, const int32_t* cand, const int32_t* seq_lens,
+                        int32_t* local, int32_t* counts, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+int dcp_sparse_decode_attention(const dcp_params* params, int32_t B, int32_t k, const void* q, const int32_t* cand,
+                                const void* k_pool, int64_t num_blocks, const int32_t* block_tables,
+                                int32_t max_blocks, const int32_t* seq_lens, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Per-rank partial decode attention ("vLLM DCP and PCP", Deep Dive 6,
  * "Deriving the partial and global outputs"): for every virtual rank r,
  * request b, query token t and head h, with s_j = softmax_scale * q . k_j over
