@@ -528,6 +528,136 @@ def run_prefill(args):
         dist.destroy_process_group()
 
 
+SPARSE_METRIC = "DCP-localised sparse MLA decode: query tokens/s and tensor roofline (top-2048 candidates, 1 GB300)"
+
+
+def run_sparse(args):
+    """Time one sparse decode pass: localisation of every query row's
+    candidates to their ranks, staging, the rank partials on the dense MLA
+    kernels and the merge."""
+    import torch
+    import context_decode_attention_gb300 as dcp
+    from context_decode_attention_gb300.harness import DeviceWorkload
+    from dcp_workloads import sparse_candidates
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name = args.workload if args.workload != DEFAULT_WORKLOAD else "mla_fp8_sparse_2k"
+    over = {"B": args.batch} if args.batch else {}
+    cfg = config(name, **over)
+    wl = make_workload(cfg, seed=int(cfg["index"]) + 1000 * rank)
+    k = int(cfg.get("topk", 2048))
+    params = dcp.params_from_config(cfg, wl.kv_scale)
+    B, Tq, Hq, Dk, Dv = (int(cfg[x]) for x in ("B", "Tq", "Hq", "Dk", "Dv"))
+    dw = DeviceWorkload(wl, device=dev, workspace_bytes=dcp.dcp_sparse_workspace_size(params, B, k))
+    cand_h = sparse_candidates(wl, k, seed=1)
+    cand = torch.from_numpy(cand_h).to(dev)
+    out = torch.empty_like(dw.out)
+    lse = torch.empty_like(dw.lse)
+    stream = dw.stream
+    peaks = load_peaks()
+    nc = int((cand_h >= 0).sum())
+    flops = 2 * nc * Hq * (Dk + Dv)
+    kv_bytes = nc * Dk * ESIZE[cfg["kv_dtype"]]
+    alg_bytes = kv_bytes + B * Tq * Hq * (Dk * 2 + Dv * 2 + 4)
+
+    def step():
+        dcp.dcp_sparse_decode_attention(dw.params, dw.q, cand, dw.k_pool, dw.num_blocks, dw.block_tables,
+                                        dw.seq_lens, out, lse, workspace=dw.workspace, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    if dw.error_bits() != 0:
+        raise SystemExit("device error bits set during warm-up")
+    steps = args.steps
+    # the candidates' rows (~75 MB) fit in L2: flush it before every timed step
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = dcp.dcp_launch_count()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.fill_(i & 255)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    launches = dcp.dcp_launch_count() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    if dw.error_bits() != 0:
+        raise SystemExit("device error bits set during the timed region")
+    ms = reduce_max([float(np.mean([a.elapsed_time(b) for a, b in ev]))], world)[0]
+
+    e2e = None
+    if not args.no_e2e:
+        q_h = dw.q.cpu().pin_memory()
+        c_h = cand.cpu().pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                dw.q.copy_(q_h, non_blocking=True)
+                cand.copy_(c_h, non_blocking=True)
+                step()
+                out_h.copy_(out, non_blocking=True)
+                lse_h.copy_(lse, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max([e0.elapsed_time(e1) / steps], world)[0]
+        e2e = {"value": world * B * Tq / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(q_h.numel() * 2 + c_h.numel() * 4),
+               "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size() + lse_h.numel() * 4),
+               "ms_per_step": e2e_ms}
+
+    t = ms / 1e3
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_mem = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tc >= t_mem:
+        roof = {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": alg_bytes / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "algorithmic_flops": flops,
+                 "algorithmic_bytes": alg_bytes, "roofline_ms": 1e3 * max(t_tc, t_mem),
+                 "peak_source": peaks["source"] + " (MEASURED_PEAKS.json, burst)",
+                 "kernel": "sparse localise + stage + mla_f8 (one virtual rank) + merges", "step_ms": ms})
+    line = {
+        "metric": SPARSE_METRIC, "value": world * B * Tq / t, "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3" if cfg["kv_dtype"] == "fp8" else "bf16",
+        "data": "synthetic (seeded; candidates from a synthetic top-k indexer)",
+        "config": dict(workload_config(cfg, wl), op="sparse", topk=k, candidates=nc,
+                       l2="flushed (256 MB write) before every timed step"),
+        "roofline": roof, "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        sample = np.full_like(cand_h, -1)
+        sample[:2] = cand_h[:2]
+        t0 = time.perf_counter()
+        oracle.sparse_attention(wl, sample)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": 2 / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": "2 query rows (x 128 heads x 2048 candidates), fp64 numpy oracle"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -539,9 +669,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling a smaller case)")
     ap.add_argument("--context", type=int, default=0, help="override to one fixed context length")
-    ap.add_argument("--op", default="decode", choices=["decode", "transfer-blocks", "prefill"],
+    ap.add_argument("--op", default="decode", choices=["decode", "transfer-blocks", "prefill", "sparse"],
                     help="decode: the decode step (default); transfer-blocks: the PD block-transfer listing; "
-                         "prefill: the PCP prefill step")
+                         "prefill: the PCP prefill step; sparse: DCP-localised top-k sparse decode")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
@@ -550,6 +680,8 @@ def main():
         return run_transfer(args)
     if args.op == "prefill":
         return run_prefill(args)
+    if args.op == "sparse":
+        return run_sparse(args)
 
     import torch
     import context_decode_attention_gb300 as dcp

@@ -379,6 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // causal bound of this query token in rank r's local positions
                 const int r = (int)((uint32_t)t.u % (uint32_t)a.N), b = (int)((uint32_t)t.u / (uint32_t)a.N);
                 bound = local_len((int64_t)a.seq_lens[b] - a.Tq + tq + 1, r, a.N, a.I);
+                // given local lengths (sparse staging) end the rank's tokens themselves
+                if (a.lens_given) bound = min(bound, (int64_t)a.local_lens[(int64_t)r * a.B + b]);
                 bound_u = t.u;
             }
             bool o_waited = false;

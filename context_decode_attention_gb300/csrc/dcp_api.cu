@@ -106,7 +106,7 @@ int run_attention(const dcp_params* params, int32_t B, const void* q, const void
                   const void* v_pool, int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks,
                   const int32_t* seq_lens, const int32_t* local_lens, bool partial_mode, float* out_partial,
                   float* lse_partial, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                  cudaStream_t stream, bool empty_ok = false) {
+                  cudaStream_t stream, bool lens_given = false) {
     int rc = validate_params(params);
     if (rc != DCP_OK) return rc;
     const dcp_params& p = *params;
@@ -138,11 +138,12 @@ int run_attention(const dcp_params* params, int32_t B, const void* q, const void
     a.q = q; a.k_pool = k_pool; a.v_pool = v_pool; a.block_tables = block_tables; a.seq_lens = seq_lens;
     a.local_lens = local_lens; a.out_partial = out_partial; a.lse_partial = lse_partial; a.out = out;
     a.lse = lse; a.ws = reinterpret_cast<uint8_t*>(workspace); a.lay = lay; a.rows = p.Tq * a.G;
+    a.lens_given = lens_given ? 1 : 0;
 
     PlanArgs pa;
     memset(&pa, 0, sizeof pa);
     pa.N = p.N; pa.I = p.I; pa.bs = p.block_size; pa.Hkv = p.Hkv; pa.Tq = p.Tq; pa.CH = a.CH; pa.B = B;
-    pa.partial_mode = a.partial_mode; pa.W = W; pa.empty_ok = empty_ok ? 1 : 0; pa.max_blocks = max_blocks; pa.seq_lens = seq_lens;
+    pa.partial_mode = a.partial_mode; pa.W = W; pa.lens_given = lens_given ? 1 : 0; pa.max_blocks = max_blocks; pa.seq_lens = seq_lens;
     pa.local_lens = local_lens; pa.ws = a.ws; pa.lay = lay; pa.U = a.U; pa.G = a.Gn;
     pa.rows_per_group = a.rows; pa.Hq = p.Hq; pa.Dv = p.Dv; pa.out_partial = out_partial;
     pa.lse_partial = lse_partial; pa.out = out; pa.lse = lse; pa.out_dtype = p.out_dtype;
@@ -175,36 +176,37 @@ int run_attention(const dcp_params* params, int32_t B, const void* q, const void
 // ---- DCP-localised sparse attention ------------------------------------------
 // Workspace: the dense pass's own workspace first (its header is the caller's
 // error word), then the localised lists, the staging cache and the partials.
+// The dense pass sees query row i as request i with Tq 1 and rank r's
+// candidates of it as rank r's local tokens: I = kpad and seq_len = N kpad
+// make every rank's closed-form length kpad, a cap the given candidate counts
+// never exceed, and every staged token visible; its fused merge over the
+// ranks is then the exact sparse result.
 struct SparseLayout {
-    size_t inner, local, counts, st_q, st_pool, st_tables, st_lens, part_o, part_lse, total;
+    size_t inner, local, counts, st_pool, st_tables, st_lens, total;
     int64_t R, S;
     int kpad;
 };
 
 bool sparse_layout(const dcp_params& p, int32_t B, int32_t k, dcp_params* inner, SparseLayout* L) {
-    *inner = p;
-    inner->N = 1;
-    inner->I = 1;
-    inner->block_size = 64;
-    inner->Tq = 1;
     L->R = (int64_t)B * p.Tq;
     L->S = L->R * p.N;
     L->kpad = (k + 63) / 64 * 64;
+    *inner = p;
+    inner->I = L->kpad;
+    inner->block_size = 64;
+    inner->Tq = 1;
     WsLayout lay;
     Kernel kern;
     int64_t W;
-    if (!layout_for(*inner, (int32_t)L->S, &lay, &kern, &W)) return false;
+    if (!layout_for(*inner, (int32_t)L->R, &lay, &kern, &W)) return false;
     const size_t esz = p.kv_dtype == DCP_FP8_E4M3 ? 1 : (p.kv_dtype == DCP_BF16 ? 2 : 4);
     size_t o = align256(lay.total);
     L->inner = lay.total;
     L->local = o; o = align256(o + sizeof(int32_t) * (size_t)(p.N * L->R * k));
     L->counts = o; o = align256(o + sizeof(int32_t) * (size_t)(p.N * L->R));
-    L->st_q = o; o = align256(o + (size_t)L->S * p.Hq * p.Dk * 2);
     L->st_pool = o; o = align256(o + (size_t)L->S * L->kpad * p.Dk * esz);
     L->st_tables = o; o = align256(o + sizeof(int32_t) * (size_t)(L->S * (L->kpad / 64)));
-    L->st_lens = o; o = align256(o + sizeof(int32_t) * (size_t)L->S);
-    L->part_o = o; o = align256(o + sizeof(float) * (size_t)L->S * p.Hq * p.Dv);
-    L->part_lse = o; o = align256(o + sizeof(float) * (size_t)L->S * p.Hq);
+    L->st_lens = o; o = align256(o + sizeof(int32_t) * (size_t)L->R);
     L->total = o;
     return true;
 }
@@ -424,30 +426,22 @@ int dcp_sparse_decode_attention(const dcp_params* params, int32_t B, int32_t k, 
     if (launch_sparse_localize(p.N, p.I, (int)L.R, p.Tq, k, cand, seq_lens, local, counts, err, stream) !=
         cudaSuccess)
         return DCP_ERR_CUDA;
-    // 2. staging: request r R + i holds rank r's candidate rows of query row i
+    // 2. staging: rank r's candidate rows of query row i, contiguous
     SparseStageArgs sa;
     memset(&sa, 0, sizeof sa);
     sa.N = p.N; sa.R = (int)L.R; sa.Tq = p.Tq; sa.B = B; sa.k = k; sa.kpad = L.kpad; sa.bs = p.block_size;
     sa.max_blocks = max_blocks; sa.num_blocks = num_blocks;
     sa.row_bytes = p.Dk * (p.kv_dtype == DCP_FP8_E4M3 ? 1 : (p.kv_dtype == DCP_BF16 ? 2 : 4));
-    sa.q_row_bytes = p.Hq * p.Dk * 2;
-    sa.local = local; sa.counts = counts; sa.block_tables = block_tables; sa.k_pool = k_pool; sa.q = q;
-    sa.st_pool = ws + L.st_pool; sa.st_q = ws + L.st_q;
+    sa.local = local; sa.counts = counts; sa.block_tables = block_tables; sa.k_pool = k_pool;
+    sa.st_pool = ws + L.st_pool;
     sa.st_tables = reinterpret_cast<int32_t*>(ws + L.st_tables);
     sa.st_lens = reinterpret_cast<int32_t*>(ws + L.st_lens);
     sa.err = err;
     if (launch_sparse_stage(sa, stream) != cudaSuccess) return DCP_ERR_CUDA;
-    // 3. the rank partials: dense decode partials with one virtual rank
-    float* part_o = reinterpret_cast<float*>(ws + L.part_o);
-    float* part_lse = reinterpret_cast<float*>(ws + L.part_lse);
-    rc = run_attention(&inner, (int32_t)L.S, sa.st_q, sa.st_pool, nullptr, L.S * (L.kpad / 64), sa.st_tables,
-                       L.kpad / 64, sa.st_lens, sa.st_lens, true, part_o, part_lse, nullptr, nullptr, workspace,
-                       L.inner, stream, /*empty_ok=*/true);
-    if (rc != DCP_OK) return rc;
-    // 4. exact LSE merge over the ranks
-    return launch_lse_merge(p.N, L.R * p.Hq, p.Dv, part_o, part_lse, out, p.out_dtype, lse, stream) == cudaSuccess
-               ? DCP_OK
-               : DCP_ERR_CUDA;
+    // 3. the dense decode pass over the staged candidates, ranks merged exactly
+    return run_attention(&inner, (int32_t)L.R, q, sa.st_pool, nullptr, L.S * (L.kpad / 64), sa.st_tables,
+                         L.kpad / 64, sa.st_lens, counts, false, nullptr, nullptr, out, lse, workspace, L.inner,
+                         stream, /*lens_given=*/true);
 }
 
 int dcp_partial_attention(const dcp_params* params, int32_t B, const void* q, const void* k_pool,

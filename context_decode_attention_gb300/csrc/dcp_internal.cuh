@@ -121,24 +121,25 @@ __host__ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3
 __device__ __forceinline__ void raise_err(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
 
 // Chunks of unit u = ((b * Hkv + kvh) * N + r) with the plan's checks:
-// seq_len < Tq -> DCP_DEV_ERR_TOKEN (no chunk; with empty_ok a seq_len of 0
-// is a legitimate empty request); a local length that differs
+// seq_len < Tq -> DCP_DEV_ERR_TOKEN (no chunk); a local length that differs
 // from the closed form -> DCP_DEV_ERR_STALE (the smaller one is used); more
 // blocks than max_blocks -> DCP_DEV_ERR_TABLE (clamped).  Errors are raised
-// only when `err` is non-null.  Lengths are int32, so 32-bit closed forms.
+// only when `err` is non-null.  With lens_given the local lengths are the
+// caller's (sparse staging: any length up to the closed form) and only the
+// cap applies.  Lengths are int32, so 32-bit closed forms.
 __device__ __forceinline__ int64_t unit_chunks(int64_t u, int N, int I, int Hkv, int B, int Tq, int bs, int CH,
                                                int max_blocks, const int32_t* seq_lens, const int32_t* local_lens,
-                                               uint32_t* err, bool empty_ok = false) {
+                                               uint32_t* err, bool lens_given = false) {
     const int r = (int)(u % N);
     const int b = (int)((u / N) / Hkv);
     const int32_t L = seq_lens[b];
     const int32_t given = local_lens[(int64_t)r * B + b];
     if (L < Tq) {
-        if (err && !(empty_ok && L == 0)) raise_err(err, DCP_DEV_ERR_TOKEN);
+        if (err) raise_err(err, DCP_DEV_ERR_TOKEN);
         return 0;
     }
     const uint32_t expect = local_len32((uint32_t)L, r, N, I);
-    if (given != (int32_t)expect && err) raise_err(err, DCP_DEV_ERR_STALE);
+    if (given != (int32_t)expect && err && !lens_given) raise_err(err, DCP_DEV_ERR_STALE);
     uint32_t n = given < 0 ? 0u : ((uint32_t)given < expect ? (uint32_t)given : expect);
     if (n / (uint32_t)bs + (n % (uint32_t)bs != 0) > (uint32_t)max_blocks) {
         if (err) raise_err(err, DCP_DEV_ERR_TABLE);
@@ -167,7 +168,7 @@ struct PlanArgs {
     int B;
     int partial_mode;  // 0: groups (b, kvh); 1: groups (b, kvh, r)
     int64_t W;         // workers of the attention kernel that follows
-    int empty_ok;      // a request of length 0 is empty, not an error (sparse staging)
+    int lens_given;    // local lengths are given, not derived (sparse staging)
     int max_blocks;
     const int32_t* seq_lens;
     const int32_t* local_lens;
@@ -204,7 +205,8 @@ struct AttnArgs {
     float* lse;
     uint8_t* ws;
     WsLayout lay;
-    int rows;  // rows per group = Tq * G
+    int rows;        // rows per group = Tq * G
+    int lens_given;  // local lengths are given (sparse staging): they also bound each rank's tokens
 };
 
 // Causal prefill of a PCP-partitioned chunk: per-rank partials of query rows
@@ -233,17 +235,15 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 // every (rank, query row) candidate list as a contiguous request
 struct SparseStageArgs {
     int N, R, Tq, B, k, kpad, bs, max_blocks;  // R = query rows (B * Tq); kpad = k rounded up to 64
-    int row_bytes, q_row_bytes;                 // cache row (Dk x element) and query row (Hq x Dk x 2)
+    int row_bytes;                              // cache row: Dk x element size
     int64_t num_blocks;
     const int32_t* local;                       // [N][R][k]
     const int32_t* counts;                      // [N][R]
     const int32_t* block_tables;                // [N][B][max_blocks]
     const void* k_pool;
-    const void* q;                              // [R][Hq][Dk]
-    void* st_pool;                              // [N R kpad] rows
-    void* st_q;                                 // [N R][Hq][Dk]
-    int32_t* st_tables;                         // [N R][kpad / 64]
-    int32_t* st_lens;                           // [N R]
+    void* st_pool;                              // [N][R][kpad] rows
+    int32_t* st_tables;                         // [N][R][kpad / 64]
+    int32_t* st_lens;                           // [R]: N kpad
     uint32_t* err;
 };
 cudaError_t launch_sparse_localize(int N, int I, int rows, int Tq, int k, const int32_t* cand, const int32_t* seq_lens,

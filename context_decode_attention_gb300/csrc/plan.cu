@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     for (int64_t base = 0; base < a.U; base += kPlanThreads) {
         const int64_t u = base + tid;
         const int64_t c = u < a.U ? unit_chunks(u, a.N, a.I, a.Hkv, a.B, a.Tq, a.bs, a.CH, a.max_blocks, a.seq_lens,
-                                                a.local_lens, &hdr->err, a.empty_ok != 0)
+                                                a.local_lens, &hdr->err, a.lens_given != 0)
                                   : 0;
         const int64_t incl = block_inclusive_scan(c, warp_tot);
         if (u < a.U) {

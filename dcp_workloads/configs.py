@@ -60,6 +60,16 @@ CONFIGS = {
         q_dtype="bf16", kv_dtype="bf16", out_dtype="bf16",
         softmax_scale=1.0 / math.sqrt(128),
     ),
+    # Sparse (top-k) MLA decode: config 4's mixed contexts, 4 query tokens per
+    # request (an MTP-style step), each attending to 2,048 selected tokens
+    # (the sparse-MLA selection size of the GLM-5.3 page), candidates from a
+    # seeded synthetic indexer.
+    "mla_fp8_sparse_2k": dict(
+        index=7, layout="mla", B=16, Tq=4, Hq=128, Hkv=1, Dk=576, Dv=512,
+        lengths=("lognormal", 67 * 1024, 0.75, 4096, 200 * 1024), N=8, I=1,
+        block_size=64, topk=2048, q_dtype="bf16", kv_dtype="fp8", out_dtype="bf16",
+        softmax_scale=1.0 / math.sqrt(192),
+    ),
 }
 
 CONFIG_ORDER = ["gqa_toy", "gqa_llama8b", "mla_bf16_32k", "mla_fp8_mixed", "mla_fp8_1m"]

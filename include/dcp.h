@@ -273,10 +273,11 @@ int dcp_prefill_attention(const dcp_params* params, int32_t B, int32_t Tq, const
  *
  * dcp_sparse_decode_attention: out[i][h][:] (params' out dtype) and lse[i][h]
  * (optional, fp32) = attention of row i's heads over its candidates only.
- * Localises the candidates, stages every (rank, row) candidate list as a
- * contiguous 64-token-paged sequence in the workspace, computes the rank
- * partials with the dense decode kernels (one virtual rank each) and merges
- * them.  q [B][Tq][Hq][Dk] bf16; k_pool / block tables / seq_lens as for
+ * Localises the candidates, stages every (rank, row) candidate list as that
+ * rank's local tokens of a contiguous 64-token-paged sequence in the
+ * workspace, and runs the dense decode kernels over it with the candidate
+ * counts as the ranks' local lengths: their exact merge over the ranks is the
+ * result.  q [B][Tq][Hq][Dk] bf16; k_pool / block tables / seq_lens as for
  * dcp_decode_attention (MLA: one latent row per token, no v_pool).  A row
  * with no candidate gets zeros and -inf.  workspace: at least
  * dcp_sparse_workspace_size bytes, zeroed once by dcp_workspace_init
