@@ -422,23 +422,21 @@ int dcp_sparse_decode_attention(const dcp_params* params, int32_t B, int32_t k, 
     int32_t* local = reinterpret_cast<int32_t*>(ws + L.local);
     int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
     uint32_t* err = &reinterpret_cast<WsHeader*>(ws)->err;
-    // 1. each rank's candidates at their local positions
-    if (launch_sparse_localize(p.N, p.I, (int)L.R, p.Tq, k, cand, seq_lens, local, counts, err, stream) !=
-        cudaSuccess)
-        return DCP_ERR_CUDA;
-    // 2. staging: rank r's candidate rows of query row i, contiguous
+    // 1. each rank's candidates at their local positions, and rank r's
+    //    candidate rows of query row i copied contiguously (staging)
     SparseStageArgs sa;
     memset(&sa, 0, sizeof sa);
-    sa.N = p.N; sa.R = (int)L.R; sa.Tq = p.Tq; sa.B = B; sa.k = k; sa.kpad = L.kpad; sa.bs = p.block_size;
-    sa.max_blocks = max_blocks; sa.num_blocks = num_blocks;
+    sa.N = p.N; sa.I = p.I; sa.R = (int)L.R; sa.Tq = p.Tq; sa.B = B; sa.k = k; sa.kpad = L.kpad;
+    sa.bs = p.block_size; sa.max_blocks = max_blocks; sa.num_blocks = num_blocks;
     sa.row_bytes = p.Dk * (p.kv_dtype == DCP_FP8_E4M3 ? 1 : (p.kv_dtype == DCP_BF16 ? 2 : 4));
+    sa.cand = cand; sa.seq_lens = seq_lens;
     sa.local = local; sa.counts = counts; sa.block_tables = block_tables; sa.k_pool = k_pool;
     sa.st_pool = ws + L.st_pool;
     sa.st_tables = reinterpret_cast<int32_t*>(ws + L.st_tables);
     sa.st_lens = reinterpret_cast<int32_t*>(ws + L.st_lens);
     sa.err = err;
     if (launch_sparse_stage(sa, stream) != cudaSuccess) return DCP_ERR_CUDA;
-    // 3. the dense decode pass over the staged candidates, ranks merged exactly
+    // 2. the dense decode pass over the staged candidates, ranks merged exactly
     return run_attention(&inner, (int32_t)L.R, q, sa.st_pool, nullptr, L.S * (L.kpad / 64), sa.st_tables,
                          L.kpad / 64, sa.st_lens, counts, false, nullptr, nullptr, out, lse, workspace, L.inner,
                          stream, /*lens_given=*/true);

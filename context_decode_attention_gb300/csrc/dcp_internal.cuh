@@ -234,20 +234,23 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 // DCP-localised sparse attention: candidate localisation and the staging of
 // every (rank, query row) candidate list as a contiguous request
 struct SparseStageArgs {
-    int N, R, Tq, B, k, kpad, bs, max_blocks;  // R = query rows (B * Tq); kpad = k rounded up to 64
-    int row_bytes;                              // cache row: Dk x element size
+    int N, I, R, Tq, B, k, kpad, bs, max_blocks;  // R = query rows (B * Tq); kpad = k rounded up to 64
+    int row_bytes;                                 // cache row: Dk x element size
     int64_t num_blocks;
-    const int32_t* local;                       // [N][R][k]
-    const int32_t* counts;                      // [N][R]
-    const int32_t* block_tables;                // [N][B][max_blocks]
+    const int32_t* cand;                           // [R][k] global positions, -1 unused
+    const int32_t* seq_lens;                       // [B]
+    int32_t* local;                                // [N][R][k] written (first counts entries)
+    int32_t* counts;                               // [N][R] written
+    const int32_t* block_tables;                   // [N][B][max_blocks]
     const void* k_pool;
-    void* st_pool;                              // [N][R][kpad] rows
-    int32_t* st_tables;                         // [N][R][kpad / 64]
-    int32_t* st_lens;                           // [R]: N kpad
+    void* st_pool;                                 // [N][R][kpad] rows
+    int32_t* st_tables;                            // [N][R][kpad / 64]
+    int32_t* st_lens;                              // [R]: N kpad
     uint32_t* err;
 };
 cudaError_t launch_sparse_localize(int N, int I, int rows, int Tq, int k, const int32_t* cand, const int32_t* seq_lens,
                                    int32_t* local, int32_t* counts, uint32_t* err, cudaStream_t s);
+// localisation and staging in one launch (one CTA per rank and row)
 cudaError_t launch_sparse_stage(const SparseStageArgs& a, cudaStream_t s);
 
 // head-tail prefill partition over K PCP ranks

@@ -17,26 +17,23 @@
 namespace dcp {
 namespace {
 
-// One CTA per (query row i, rank rr): warp w scans a contiguous slice of the
-// candidate list; the warps' counts give each slice its first output slot,
-// and a second scan writes the rank's candidates in list order.
+// Rank rr's candidates of query row i, by one CTA of kLocWarps warps: warp w
+// scans a contiguous slice of the candidate list; the warps' counts give each
+// slice its first output slot, and a second scan writes the rank's
+// candidates' local positions in list order.  Returns the count (every
+// thread); fill_tail writes -1 past it.
 constexpr int kLocWarps = 8;
 
-__global__ void __launch_bounds__(32 * kLocWarps) sparse_localize_kernel(int N, int I, int rows, int Tq, int k,
-                                                                         const int32_t* __restrict__ cand,
-                                                                         const int32_t* __restrict__ seq_lens,
-                                                                         int32_t* __restrict__ local,
-                                                                         int32_t* __restrict__ counts, uint32_t* err) {
+__device__ int localize_cta(int N, int I, int Tq, int k, int64_t i, int rr, const int32_t* __restrict__ cand,
+                            const int32_t* __restrict__ seq_lens, int32_t* __restrict__ out, bool fill_tail,
+                            uint32_t* err) {
     __shared__ int s_cnt[kLocWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t i = blockIdx.x / N;
-    const int rr = (int)(blockIdx.x % N);
     const int b = (int)(i / Tq), t = (int)(i % Tq);
     const int64_t vis = (int64_t)seq_lens[b] - Tq + t + 1;  // positions this query token may see
     const int slice = (k + kLocWarps - 1) / kLocWarps;
     const int j_beg = min(k, warp * slice), j_end = min(k, j_beg + slice);
     const int32_t* row = cand + i * k;
-    int32_t* out = local + ((int64_t)rr * rows + i) * k;
     auto owner = [&](int j, int32_t& lp) -> bool {  // candidate j is rank rr's; lp = its local position
         const int32_t tok = j < j_end ? row[j] : -1;
         if (tok < 0 || tok >= vis) {
@@ -67,36 +64,83 @@ __global__ void __launch_bounds__(32 * kLocWarps) sparse_localize_kernel(int N, 
         if (own) out[base + __popc(m & ((1u << lane) - 1u))] = lp;
         base += __popc(m);
     }
-    for (int j = total + threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
+    if (fill_tail)
+        for (int j = total + threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
+    return total;
+}
+
+// One CTA per (query row i, rank rr).
+__global__ void __launch_bounds__(32 * kLocWarps) sparse_localize_kernel(int N, int I, int rows, int Tq, int k,
+                                                                         const int32_t* __restrict__ cand,
+                                                                         const int32_t* __restrict__ seq_lens,
+                                                                         int32_t* __restrict__ local,
+                                                                         int32_t* __restrict__ counts, uint32_t* err) {
+    const int64_t i = blockIdx.x / N;
+    const int rr = (int)(blockIdx.x % N);
+    const int total = localize_cta(N, I, Tq, k, i, rr, cand, seq_lens, local + ((int64_t)rr * rows + i) * k, true, err);
     if (threadIdx.x == 0) counts[(int64_t)rr * rows + i] = total;
 }
 
-// One CTA per staging request s = r R + i: its page table, and rank r's
-// candidate rows of query row i copied contiguously (16-byte pieces).
-__global__ void sparse_stage_kernel(SparseStageArgs a) {
+// One CTA per staging request s = r R + i: rank r's candidates of query row i
+// localised (as above; the positions go through the workspace, read back by
+// the same CTA), the request's page table, and the candidate rows copied
+// contiguously in 16-byte pieces.  The rows' pool offsets are resolved into
+// shared memory a batch at a time, so the copy loop has no dependent loads
+// and keeps kUnroll pieces per thread in flight.
+constexpr int kStageThreads = 32 * kLocWarps;
+constexpr int kStageBatch = 1024;  // candidate rows per batch
+constexpr int kUnroll = 4;
+
+__global__ void __launch_bounds__(kStageThreads) sparse_stage_kernel(SparseStageArgs a) {
+    __shared__ int64_t s_row[kStageBatch];
     const int64_t s = blockIdx.x;
     const int r = (int)(s / a.R);
     const int64_t i = s % a.R;
     const int b = (int)(i / a.Tq);
+    int32_t* loc = a.local + s * a.k;
+    const int cnt = localize_cta(a.N, a.I, a.Tq, a.k, i, r, a.cand, a.seq_lens, loc, false, a.err);
+    if (threadIdx.x == 0) a.counts[s] = cnt;
     const int pages = a.kpad / 64;
-    for (int p = threadIdx.x; p < pages; p += blockDim.x) a.st_tables[s * pages + p] = (int32_t)(s * pages + p);
+    for (int p = threadIdx.x; p < pages; p += kStageThreads) a.st_tables[s * pages + p] = (int32_t)(s * pages + p);
     if (r == 0 && threadIdx.x == 0) a.st_lens[i] = a.N * a.kpad;
-    const int cnt = a.counts[s];
     const int vec = a.row_bytes / 16;
-    const int32_t* loc = a.local + s * a.k;
-    const int32_t* bt = a.block_tables + ((int64_t)r * a.B + b) * a.max_blocks;
-    const uint4* src = reinterpret_cast<const uint4*>(a.k_pool);
-    uint4* dst = reinterpret_cast<uint4*>(a.st_pool) + s * a.kpad * vec;
+    const int32_t* __restrict__ bt = a.block_tables + ((int64_t)r * a.B + b) * a.max_blocks;
+    const uint4* __restrict__ src = reinterpret_cast<const uint4*>(a.k_pool);
+    uint4* __restrict__ dst = reinterpret_cast<uint4*>(a.st_pool) + s * a.kpad * vec;
     bool bad = false;
-    for (int x = threadIdx.x; x < cnt * vec; x += blockDim.x) {
-        const int j = x / vec, v = x - j * vec;
-        const int32_t lp = loc[j];
-        const int32_t blk = bt[lp / a.bs];
-        if (blk < 0 || blk >= a.num_blocks) {
-            bad = true;
-            continue;
+    for (int j0 = 0; j0 < cnt; j0 += kStageBatch) {
+        const int nb = min(kStageBatch, cnt - j0);
+        __syncthreads();  // the localised positions are written; the previous batch's offsets are read
+        for (int j = threadIdx.x; j < nb; j += kStageThreads) {
+            const int32_t lp = loc[j0 + j];
+            const int32_t blk = bt[lp / a.bs];
+            const bool ok = blk >= 0 && blk < a.num_blocks;
+            bad |= !ok;
+            s_row[j] = ok ? ((int64_t)blk * a.bs + lp % a.bs) * vec : -1;
         }
-        dst[(int64_t)j * vec + v] = src[((int64_t)blk * a.bs + lp % a.bs) * vec + v];
+        __syncthreads();
+        const int tot = nb * vec;
+        uint4* __restrict__ d0 = dst + (int64_t)j0 * vec;
+        for (int x0 = threadIdx.x; x0 < tot; x0 += kUnroll * kStageThreads) {
+            uint4 val[kUnroll];
+            int at[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int x = x0 + u * kStageThreads;
+                at[u] = -1;
+                if (x < tot) {
+                    const int j = x / vec, c = x - j * vec;
+                    const int64_t o = s_row[j];
+                    if (o >= 0) {
+                        val[u] = src[o + c];
+                        at[u] = x;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+                if (at[u] >= 0) d0[at[u]] = val[u];
+        }
     }
     if (bad) raise_err(a.err, DCP_DEV_ERR_BLOCK_ID);
 }
@@ -112,7 +156,7 @@ cudaError_t launch_sparse_localize(int N, int I, int rows, int Tq, int k, const 
 }
 
 cudaError_t launch_sparse_stage(const SparseStageArgs& a, cudaStream_t s) {
-    sparse_stage_kernel<<<(unsigned)((int64_t)a.N * a.R), 256, 0, s>>>(a);
+    sparse_stage_kernel<<<(unsigned)((int64_t)a.N * a.R), kStageThreads, 0, s>>>(a);
     count_launches(1);
     return cudaGetLastError();
 }

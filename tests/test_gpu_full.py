@@ -67,3 +67,88 @@ def test_full_size(name):
     rows = _sample_rows(wl, 12, seed=7)
     ref_o, ref_l = oracle.attention(wl, rows=rows)
     assert_close_rows(out_h[rows], lse_h[rows], ref_o, ref_l, tol_for(c), f"{name} sampled rows")
+
+
+def test_full_size_prefill():
+    """The PCP prefill workload (2 x a 2K chunk on a 64K context, PCP 4 x DCP 4,
+    64-token pages) exactly as the bench runs it: partition bit-exact, merged
+    rows sampled across the chunk (both ends, the head-tail split points, random
+    tokens) against the oracle's causal attention of those rows."""
+    from context_decode_attention_gb300.harness import DeviceWorkload
+    cfg = config("gqa_prefill_64k")
+    wl = make_workload(cfg, seed=int(cfg["index"]))
+    dw = DeviceWorkload(wl, workspace_bytes=256)
+    K = int(cfg["pcp"])
+    dw.prefill_setup(K)
+    B, Tq, Hq = int(cfg["B"]), int(cfg["Tq"]), int(cfg["Hq"])
+    for _ in range(2):
+        dw.write_new_tokens()
+        out, lse = dw.prefill()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    ref = oracle.pcp_partition(K, wl.seq_lens - Tq, np.full(B, Tq), dw.max_q)
+    assert np.array_equal(dw.q_pos.cpu().numpy(), ref["pos"])
+    pos = ref["pos"].astype(np.int64)
+    ctx = wl.seq_lens.astype(np.int64) - Tq
+    rng = np.random.default_rng(11)
+    piece = Tq // (2 * K)
+    toks = sorted(set([0, Tq - 1] + [p * piece for p in range(2 * K)] + [p * piece - 1 for p in range(1, 2 * K)]
+                      + rng.integers(0, Tq, size=16).tolist()))
+    picks = []  # (b, gathered index, natural token, head)
+    for b in range(B):
+        where = {int(p - ctx[b]): j for j, p in enumerate(pos[b]) if p >= 0}
+        assert sorted(where) == list(range(Tq))
+        for t in toks:
+            for h in sorted({int(rng.integers(0, Hq)), (7 * t + b) % Hq}):
+                picks.append((b, where[t], t, h))
+    rows = np.array([(b * Tq + t) * Hq + h for b, _, t, h in picks], dtype=np.int64)
+    ref_o, ref_l = oracle.attention(wl, rows=rows)
+    got_o, got_l = f64(out), f64(lse)
+    bi = np.array([p[0] for p in picks])
+    ji = np.array([p[1] for p in picks])
+    hi = np.array([p[3] for p in picks])
+    assert_close_rows(got_o[bi, ji, hi], got_l[bi, ji, hi], ref_o, ref_l, tol_for(cfg), "prefill sampled rows")
+
+
+def test_full_size_sparse():
+    """The sparse workload (config 4's contexts, 4 query tokens per request,
+    2,048 candidates per token) exactly as the bench runs it: localisation
+    bit-exact for every row, merged output of sampled query tokens (all heads)
+    against the oracle's attention over their candidates."""
+    import context_decode_attention_gb300 as dcp
+    from context_decode_attention_gb300.harness import DeviceWorkload
+    from dcp_workloads import sparse_candidates
+    cfg = config("mla_fp8_sparse_2k")
+    wl = make_workload(cfg, seed=int(cfg["index"]))
+    k = int(cfg["topk"])
+    params = dcp.params_from_config(cfg, wl.kv_scale)
+    B, Tq, N = int(cfg["B"]), int(cfg["Tq"]), int(cfg["N"])
+    dw = DeviceWorkload(wl, workspace_bytes=dcp.dcp_sparse_workspace_size(params, B, k))
+    cand_h = sparse_candidates(wl, k, seed=1)
+    cand = torch.from_numpy(cand_h).cuda()
+    out = torch.empty_like(dw.out)
+    lse = torch.empty_like(dw.lse)
+    for _ in range(2):
+        dcp.dcp_sparse_decode_attention(dw.params, dw.q, cand, dw.k_pool, dw.num_blocks, dw.block_tables,
+                                        dw.seq_lens, out, lse, workspace=dw.workspace)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    rows = B * Tq
+    local = torch.full((N, rows, k), -7, dtype=torch.int32, device="cuda")
+    counts = torch.full((N, rows), -7, dtype=torch.int32, device="cuda")
+    dcp.dcp_sparse_localize(dw.params, cand, dw.seq_lens, local, counts, workspace=dw.workspace)
+    ref_local, ref_counts = oracle.sparse_localize(cand_h, N, int(cfg["I"]), wl.seq_lens, Tq)
+    assert np.array_equal(counts.cpu().numpy(), ref_counts)
+    assert np.array_equal(local.cpu().numpy(), ref_local)
+    # sampled query tokens: the longest and the shortest request, random others
+    rng = np.random.default_rng(5)
+    b_long, b_short = int(np.argmax(wl.seq_lens)), int(np.argmin(wl.seq_lens))
+    pick = sorted({b_long * Tq + Tq - 1, b_short * Tq, *rng.integers(0, rows, size=4).tolist()})
+    sub = np.full_like(cand_h, -1)
+    sub[pick] = cand_h[pick]
+    ref_o, ref_l = oracle.sparse_attention(wl, sub)
+    Hq = int(cfg["Hq"])
+    sel = np.concatenate([np.arange(i * Hq, (i + 1) * Hq) for i in pick])
+    got_o = f64(out).reshape(ref_o.shape)
+    got_l = f64(lse).reshape(-1)
+    assert_close_rows(got_o[sel], got_l[sel], ref_o[sel], ref_l[sel], tol_for(cfg), "sparse sampled tokens")
