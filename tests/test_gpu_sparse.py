@@ -18,7 +18,22 @@ CASES = {
     "fp8_mixed_k256": (config("mla_fp8_mixed", B=3, lengths=("list", [700, 3000, 90])), 256),
     "bf16_tq2_k128_I64": (config("mla_bf16_32k", B=2, Tq=2, lengths=("list", [1500, 50])), 128),
     "fp8_n3_i5_k512": (config("mla_fp8_mixed", B=2, N=3, I=5, lengths=("list", [4000, 600])), 512),
+    # k not a multiple of the 64-token staging page; an empty row, a short
+    # list, an unsorted list (see _edit)
+    "fp8_n2_k100_ragged": (config("mla_fp8_mixed", B=3, Tq=2, N=2, lengths=("list", [900, 40, 3000])), 100),
+    # one rank: the sparse result without any merge
+    "bf16_n1_k64": (config("mla_bf16_32k", B=2, N=1, I=1, lengths=("list", [64, 500])), 64),
 }
+
+
+def _edit(name, cand):
+    """Candidate lists the synthetic indexer does not produce by itself."""
+    if name == "fp8_n2_k100_ragged":
+        cand = cand.copy()
+        cand[1] = -1             # no candidate at all: zeros and -inf
+        cand[3, 10:] = -1        # ten candidates
+        cand[4] = cand[4][::-1]  # descending order (the result does not depend on it)
+    return cand
 
 _cache = {}
 
@@ -32,7 +47,7 @@ def _setup(name):
         params = dcp.params_from_config(cfg, wl.kv_scale)
         ws = dcp.dcp_sparse_workspace_size(params, int(cfg["B"]), k)
         dw = DeviceWorkload(wl, workspace_bytes=ws)
-        cand = sparse_candidates(wl, k, seed=1)
+        cand = _edit(name, sparse_candidates(wl, k, seed=1))
         _cache.clear()
         _cache[name] = (wl, dw, cand, k)
     return _cache[name]
