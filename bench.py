@@ -58,8 +58,8 @@ MEASURED_TRAFFIC = {
     ("transfer_blocks", "entry"): ("transfer.cu", "ba69fc5af5bf509387a4668d62e0fd322f75cc04daf9e1105750d478aee93893",
                                    (161.792e3 + 0.0) / (8 * 16 * 284)),
     # per request of the prefill workload's shape (2K chunk on a 64K context)
-    ("prefill", "request"): ("attn_prefill_tc.cu", "8608f7c006c096a93a90bbcbcbf098974209e440eb6f9480f60e124e04491360",
-                             294.589440e6 + 112.330240e6),
+    ("prefill", "request"): ("attn_prefill_tc.cu", "af72f7fa8e7fd134470c2e65d432981492e1481398585f4304da26fcb4612426",
+                             294.779904e6 + 112.346112e6),
 }
 
 

@@ -124,6 +124,12 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
     return d;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -405,26 +411,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sbase = tm + 128 + 128 * sb + lane_off + c0;
             // columns [0, lim) of this group's 64 are visible to the row
             const int lim = max(0, min(kGroupCols, bound - t * kKeys - c0));
-            float mraw = -INFINITY;
-            {
-                uint32_t rr[32];
-#pragma unroll 1
-                for (int c = 0; c < kGroupCols / 32; ++c) {
-                    tmem_ld32(sbase + 32 * c, rr);
-                    tmem_wait_ld();
-                    const int lc = lim - 32 * c;
-                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                    if (lc >= 32) {
+            // the group's 64 scores stay in registers for both passes; the
+            // columns past the row's bound (diagonal tiles only) become -inf
+            static_assert(kGroupCols == 64, "two 32-column loads per group");
+            uint32_t sv0[32], sv1[32];
+            tmem_ld32(sbase, sv0);
+            tmem_ld32(sbase + 32, sv1);
+            tmem_wait_ld();
+#define SV(k) ((k) < 32 ? sv0[(k) & 31] : sv1[(k) & 31])
+            if (lim < kGroupCols) {
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(rr[k]));
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            m4[k & 3] = fmaxf(m4[k & 3], (k < lc) ? __uint_as_float(rr[k]) : -INFINITY);
-                    }
-                    mraw = fmaxf(mraw, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
-                }
+                for (int k = 0; k < kGroupCols; ++k)
+                    if (k >= lim) SV(k) = 0xff800000u;
             }
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int k = 0; k < kGroupCols; k += 2)
+                m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(SV(k)), __uint_as_float(SV(k + 1)));
+            const float mraw = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
             s_xch[grp][h] = (lim > 0) ? mraw * sl2 : -INFINITY;
             if (!both(1, ok)) { alive = false; break; }
             float mx = s_xch[0][h];  // the row's max over the tile (base 2)
@@ -444,47 +448,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            // P as bf16 pairs over the group's first 32 columns; the exponential
-            // pass is bound by instruction issue, so a tile's fully visible
-            // 16-column steps take packed fp32x2 arithmetic and no mask
-            // (5.05 -> 4.39 ms on the 64K-context prefill workload)
-            float lsum = 0.f;
-#pragma unroll 1
+            // P as bf16 pairs over the group's first 32 columns.  The pass is
+            // bound by instruction issue, not by the SFU (moving 1/8 or 1/4 of
+            // the exponentials to an FMA-pipe polynomial made it slower): scale,
+            // shift and sum go two columns per instruction (fp32x2), and the
+            // scores come from registers
+            uint64_t acc = pair_f32(0.f, 0.f);
+            const uint64_t sc = pair_f32(sl2, sl2), mu = pair_f32(nmu, nmu);
+#pragma unroll
             for (int q = 0; q < kGroupCols / 16; ++q) {
-                uint32_t r16[16], pk[8];
-                tmem_ld16(sbase + 16 * q, r16);
-                tmem_wait_ld();
-                const int lq = lim - 16 * q;
-                float ls2[2] = {0.f, 0.f};
-                if (lq >= 16) {
-                    // every column visible: scale, shift and sum two columns per instruction
-                    uint64_t acc = pair_f32(0.f, 0.f);
-                    const uint64_t sc = pair_f32(sl2, sl2), mu = pair_f32(nmu, nmu);
+                uint32_t pk[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float x0, x1;
-                        unpair_f32(fma_f32x2(pair_f32(__uint_as_float(r16[2 * k]), __uint_as_float(r16[2 * k + 1])),
-                                             sc, mu),
-                                   x0, x1);
-                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        acc = add_f32x2(acc, pair_f32(p0, p1));
-                        pk[k] = pack_bf16(p0, p1);
-                    }
-                    unpair_f32(acc, ls2[0], ls2[1]);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float s0 = (2 * k < lq) ? __uint_as_float(r16[2 * k]) : -INFINITY;
-                        const float s1 = (2 * k + 1 < lq) ? __uint_as_float(r16[2 * k + 1]) : -INFINITY;
-                        const float p0 = ex2_approx(fmaf(s0, sl2, nmu)), p1 = ex2_approx(fmaf(s1, sl2, nmu));
-                        ls2[0] += p0;
-                        ls2[1] += p1;
-                        pk[k] = pack_bf16(p0, p1);
-                    }
+                for (int k = 0; k < 8; ++k) {
+                    float x0, x1;
+                    unpair_f32(fma_f32x2(pair_f32(__uint_as_float(SV(16 * q + 2 * k)),
+                                                  __uint_as_float(SV(16 * q + 2 * k + 1))),
+                                         sc, mu),
+                               x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    acc = add_f32x2(acc, pair_f32(p0, p1));
+                    pk[k] = pack_bf16(p0, p1);
                 }
-                lsum += ls2[0] + ls2[1];
                 tmem_st8(sbase + 8 * q, pk);
             }
+#undef SV
+            float ls0, ls1;
+            unpair_f32(acc, ls0, ls1);
+            const float lsum = ls0 + ls1;
             l = (corr == 0.f ? 0.f : l * corr) + lsum;
             // P.V of the previous tile must be complete before O is touched;
             // the second barrier also keeps s_xch from being overwritten early
