@@ -48,18 +48,18 @@ def load_peaks():
 # the launch's cached tokens; summaries and commands under profiles/).  Valid
 # only for the kernel source they were taken on: a changed source gives null.
 MEASURED_TRAFFIC = {
-    ("mla_tcgen05", "fp8"): ("attn_mla_f8.cu", "baaa1f173833ec151d8ab6e873e30be305418562a436fb184dd229e866cc3d05",
-                             (219.019520e6 + 4.405504e6) / 376734),
-    ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "92ce2ed12a639aa71b9b45dcdfffcdcb79b08359f9b7301c8c23865a7b269409",
-                              (304.013568e6 + 4.242944e6) / 262144),
+    ("mla_tcgen05", "fp8"): ("attn_mla_f8.cu", "68b98a09f8e5560d3bbee06ef8a324c2df3491fe79ef40ecf54a78e24efaeed5",
+                             (218.994944e6 + 4.241664e6) / 376734),
+    ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "f181fb50cf28a8417ae8e36123311d16e8c6be1de275ebd7dc8aacc7be4b9dea",
+                              (304.078336e6 + 4.367360e6) / 262144),
     ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "55f1cce0d8111ec459e79dfdc0f0496849629421f35c1b418f54f7e664fe62df",
                           (268.632576e6 + 3.230976e6) / 65536),
     # per table entry (N B max_blocks) of the block-transfer listing
     ("transfer_blocks", "entry"): ("transfer.cu", "ba69fc5af5bf509387a4668d62e0fd322f75cc04daf9e1105750d478aee93893",
                                    (161.792e3 + 0.0) / (8 * 16 * 284)),
     # per request of the prefill workload's shape (2K chunk on a 64K context)
-    ("prefill", "request"): ("attn_prefill_tc.cu", "af72f7fa8e7fd134470c2e65d432981492e1481398585f4304da26fcb4612426",
-                             294.779904e6 + 112.346112e6),
+    ("prefill", "request"): ("attn_prefill_tc.cu", "b11be23ad86943e87c64b65bc737101d7478d5d2015727aedd6a4bed7851b06e",
+                             294.617600e6 + 112.390912e6),
 }
 
 

@@ -557,10 +557,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
                 const int lc = lim - 32 * c;
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (lc >= 32) {  // every column visible: no mask, three-input max
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    m4[k & 3] = fmaxf(m4[k & 3], (k < lc) ? __uint_as_float(rr[k]) : -INFINITY);
-                mraw = fmaxf(mraw, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                    for (int k = 0; k < 32; k += 2)
+                        m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(rr[k]), __uint_as_float(rr[k + 1]));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        m4[k & 3] = fmaxf(m4[k & 3], (k < lc) ? __uint_as_float(rr[k]) : -INFINITY);
+                }
+                mraw = fmax3(mraw, fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
             const float mx = (lim > 0) ? mraw * sl2h : -INFINITY;
             float corr = 1.f;
@@ -578,8 +584,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float nb = (m_ref == -INFINITY) ? 0.f : kPBias - m_ref;
             // pass 2: 16 columns at a time, p' = 2^(s sl2h + nb) split into hi/lo;
             // chunk c's hi/lo go over its own first 16 columns (hi in [32 c,
-            // 32 c + 8), lo in [32 c + 8, 32 c + 16)), after they are read
+            // 32 c + 8), lo in [32 c + 8, 32 c + 16)), after they are read.
+            // Fully visible steps take no mask and scale, shift and sum two
+            // columns per instruction (these warps are issue-bound)
             float lsum = 0.f;
+            const uint64_t sc2 = pair_f32(sl2h, sl2h), nb2 = pair_f32(nb, nb);
 #pragma unroll 1
             for (int qq = 0; qq < 2 * nchunks; ++qq) {
                 uint32_t r16[16];
@@ -588,16 +597,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int lq = lim - 16 * qq;
                 uint32_t hw[4], lw[4];
                 float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+                if (lq >= 16) {
+                    // every column visible: scale, shift and sum two columns per instruction
+                    uint64_t a01 = pair_f32(0.f, 0.f), a23 = pair_f32(0.f, 0.f);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float p[4];
+                    for (int k = 0; k < 4; ++k) {
+                        float x[4];
+                        unpair_f32(fma_f32x2(pair_f32(__uint_as_float(r16[4 * k]), __uint_as_float(r16[4 * k + 1])),
+                                             sc2, nb2),
+                                   x[0], x[1]);
+                        unpair_f32(fma_f32x2(pair_f32(__uint_as_float(r16[4 * k + 2]),
+                                                      __uint_as_float(r16[4 * k + 3])),
+                                             sc2, nb2),
+                                   x[2], x[3]);
+                        float p[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float sc = (4 * k + e < lq) ? __uint_as_float(r16[4 * k + e]) : -INFINITY;
-                        p[e] = ex2_approx(fmaf(sc, sl2h, nb));
-                        ls4[e] += p[e];
+                        for (int e = 0; e < 4; ++e) p[e] = ex2_approx(x[e]);
+                        a01 = add_f32x2(a01, pair_f32(p[0], p[1]));
+                        a23 = add_f32x2(a23, pair_f32(p[2], p[3]));
+                        split4(p[0], p[1], p[2], p[3], hw[k], lw[k]);
                     }
-                    split4(p[0], p[1], p[2], p[3], hw[k], lw[k]);
+                    unpair_f32(a01, ls4[0], ls4[1]);
+                    unpair_f32(a23, ls4[2], ls4[3]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float p[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float sc = (4 * k + e < lq) ? __uint_as_float(r16[4 * k + e]) : -INFINITY;
+                            p[e] = ex2_approx(fmaf(sc, sl2h, nb));
+                            ls4[e] += p[e];
+                        }
+                        split4(p[0], p[1], p[2], p[3], hw[k], lw[k]);
+                    }
                 }
                 lsum += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
                 const uint32_t col = sbase + 32 * (qq >> 1) + 4 * (qq & 1);

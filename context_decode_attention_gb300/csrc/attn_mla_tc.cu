@@ -413,10 +413,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_ld();
                     const int lc = lim - 32 * c;
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    if (lc >= 32) {  // every column visible: no mask, three-input max
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        m4[k & 3] = fmaxf(m4[k & 3], (k < lc) ? __uint_as_float(rr[k]) : -INFINITY);
-                    mraw = fmaxf(mraw, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                        for (int k = 0; k < 32; k += 2)
+                            m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(rr[k]), __uint_as_float(rr[k + 1]));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            m4[k & 3] = fmaxf(m4[k & 3], (k < lc) ? __uint_as_float(rr[k]) : -INFINITY);
+                    }
+                    mraw = fmax3(mraw, fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 }
             }
             const float mx = (lim > 0) ? mraw * sl2 : -INFINITY;
@@ -435,8 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
             // pass 2: 16 columns at a time; their bf16 pairs go to columns
-            // [8 q, 8 q + 8), which earlier steps have already read
+            // [8 q, 8 q + 8), which earlier steps have already read.  The
+            // softmax warps are bound by instruction issue: fully visible steps
+            // take no mask and scale, shift and sum two columns per instruction
+            // (a second softmax warpgroup over half of the columns, with the
+            // row maxima exchanged at a barrier, was slower)
             float lsum = 0.f;
+            const uint64_t sc2 = pair_f32(sl2, sl2), mu2 = pair_f32(nmu, nmu);
 #pragma unroll 1
             for (int q = 0; q < ncols / 16; ++q) {
                 uint32_t r16[16], pk[8];
@@ -444,14 +455,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
                 const int lq = lim - 16 * q;
                 float ls2[2] = {0.f, 0.f};
+                if (lq >= 16) {
+                    // every column visible: scale, shift and sum two columns per instruction
+                    uint64_t acc = pair_f32(0.f, 0.f);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float s0 = (2 * k < lq) ? __uint_as_float(r16[2 * k]) : -INFINITY;
-                    const float s1 = (2 * k + 1 < lq) ? __uint_as_float(r16[2 * k + 1]) : -INFINITY;
-                    const float p0 = ex2_approx(fmaf(s0, sl2, nmu)), p1 = ex2_approx(fmaf(s1, sl2, nmu));
-                    ls2[0] += p0;
-                    ls2[1] += p1;
-                    pk[k] = pack_bf16(p0, p1);
+                    for (int k = 0; k < 8; ++k) {
+                        float x0, x1;
+                        unpair_f32(fma_f32x2(pair_f32(__uint_as_float(r16[2 * k]), __uint_as_float(r16[2 * k + 1])),
+                                             sc2, mu2),
+                                   x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        acc = add_f32x2(acc, pair_f32(p0, p1));
+                        pk[k] = pack_bf16(p0, p1);
+                    }
+                    unpair_f32(acc, ls2[0], ls2[1]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float s0 = (2 * k < lq) ? __uint_as_float(r16[2 * k]) : -INFINITY;
+                        const float s1 = (2 * k + 1 < lq) ? __uint_as_float(r16[2 * k + 1]) : -INFINITY;
+                        const float p0 = ex2_approx(fmaf(s0, sl2, nmu)), p1 = ex2_approx(fmaf(s1, sl2, nmu));
+                        ls2[0] += p0;
+                        ls2[1] += p1;
+                        pk[k] = pack_bf16(p0, p1);
+                    }
                 }
                 lsum += ls2[0] + ls2[1];
                 tmem_st8(sbase + 8 * q, pk);
