@@ -65,8 +65,8 @@ constexpr int kOffBar = kOffRing + kStages * kStageBytes;
 constexpr int kNumBars = 2 * kStages + 1 + 2 + 2 + 1;
 constexpr int kOffKv = kOffBar + kNumBars * 8 + 16;     // after the barriers and the TMEM address
 constexpr int kOffBlk = kOffKv + 16;                    // [kProd][32] block ids of the producers' current tile
-constexpr int kOffXch = kOffBlk + kProd * 32 * 4;       // [kSoftGroups][kRows] floats
-constexpr int kSmem = kOffXch + kSoftGroups * kRows * 4;
+constexpr int kOffXch = kOffBlk + kProd * 32 * 4;       // [2][kSoftGroups][kRows] floats
+constexpr int kSmem = kOffXch + 2 * kSoftGroups * kRows * 4;
 static_assert(kSmem <= 232448, "shared memory");
 
 struct Bars {
@@ -120,7 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Bars sh = carve(smem);
     int& s_kv = *reinterpret_cast<int*>(smem + kOffKv);
     int32_t(*s_blk)[32] = reinterpret_cast<int32_t(*)[32]>(smem + kOffBlk);
-    float(*s_xch)[kRows] = reinterpret_cast<float(*)[kRows]>(smem + kOffXch);  // groups' row maxima, then sums
+    // the groups' row maxima (then row sums), double-buffered by tile parity:
+    // a buffer is rewritten only after the next exchange barrier, which every
+    // thread passes after reading it
+    float(*s_xch2)[kSoftGroups][kRows] = reinterpret_cast<float(*)[kSoftGroups][kRows]>(smem + kOffXch);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
@@ -378,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : "memory");
             return out != 0;
         };
+        bool ok_prev = true;
         for (int t = 0; t < ntiles; ++t) {
             const int sb = t & 1;
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&sh.s_full[sb], (t >> 1) & 1));
@@ -403,8 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < kGroupCols; k += 2)
                 m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(SV(k)), __uint_as_float(SV(k + 1)));
             const float mraw = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+            float(*s_xch)[kRows] = s_xch2[t & 1];
             s_xch[grp][h] = (lim > 0) ? mraw * sl2 : -INFINITY;
-            if (!both(1, ok)) { alive = false; break; }
+            // the exchange barrier also carries the previous tile's o_done outcome
+            if (!both(1, ok && ok_prev)) { alive = false; break; }
             float mx = s_xch[0][h];  // the row's max over the tile (base 2)
 #pragma unroll
             for (int g = 1; g < kSoftGroups; ++g) mx = fmaxf(mx, s_xch[g][h]);
@@ -450,11 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             unpair_f32(acc, ls0, ls1);
             const float lsum = ls0 + ls1;
             l = (corr == 0.f ? 0.f : l * corr) + lsum;
-            // P.V of the previous tile must be complete before O is touched;
-            // the second barrier also keeps s_xch from being overwritten early
-            bool ok2 = true;
-            if (t > 0) ok2 = __all_sync(0xffffffffu, mbar_wait(sh.o_done, (t - 1) & 1));
-            if (!both(2, ok2)) { alive = false; break; }
+            // P.V of the previous tile must be complete before O is touched
+            // (the outcome joins the next exchange barrier's flag)
+            if (t > 0) ok_prev = __all_sync(0xffffffffu, mbar_wait(sh.o_done, (t - 1) & 1));
             tc_fence_after();
             if (__any_sync(0xffffffffu, rescale_o)) {
                 const float f = rescale_o ? corr : 1.f;
@@ -477,8 +481,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the row's normalised partial (and, group 0, the LSE)
         bool ok3 = alive;
         if (alive && ntiles > 0) ok3 = __all_sync(0xffffffffu, mbar_wait(sh.o_done, (ntiles - 1) & 1));
+        float(*s_xch)[kRows] = s_xch2[ntiles & 1];
         s_xch[grp][h] = l;
-        const bool read_o = both(1, ok3) && ntiles > 0;  // uniform across both groups
+        const bool read_o = both(1, ok3 && ok_prev) && ntiles > 0;  // uniform across both groups
         tc_fence_after();
         float lt = s_xch[0][h];
 #pragma unroll
