@@ -58,8 +58,8 @@ MEASURED_TRAFFIC = {
     ("transfer_blocks", "entry"): ("transfer.cu", "ba69fc5af5bf509387a4668d62e0fd322f75cc04daf9e1105750d478aee93893",
                                    (161.792e3 + 0.0) / (8 * 16 * 284)),
     # per request of the prefill workload's shape (2K chunk on a 64K context)
-    ("prefill", "request"): ("attn_prefill_tc.cu", "b11be23ad86943e87c64b65bc737101d7478d5d2015727aedd6a4bed7851b06e",
-                             294.617600e6 + 112.390912e6),
+    ("prefill", "request"): ("attn_prefill_tc.cu", "0ca33f85d5d7aaa267d27097bc8aa7f3af4c0300056cb3163d6de4e6637a2f9f",
+                             294.613248e6 + 112.225280e6),
 }
 
 
