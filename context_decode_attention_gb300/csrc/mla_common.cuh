@@ -37,7 +37,8 @@ __device__ __forceinline__ int64_t cache_units(int64_t* us_s, const int64_t* us,
     return n;
 }
 
-// The same tile sequence in every role: walk the worker's chunk range; a tile
+// The same tile sequence in every role (host-callable too, for the CPU check
+// of the walk): walk the worker's chunk range; a tile
 // is up to two consecutive chunks of one unit.  `first` / `last` mark the
 // tiles that open and close a merge group inside the range.
 struct TileCursor {
@@ -47,17 +48,17 @@ struct TileCursor {
     int64_t c, c1, u, ubeg, uend;  // current chunk, range end, unit and its chunk range
     int64_t prev_group;
     int N, partial;
-    __device__ void init(const int64_t* us_, const int64_t* us_s_, int64_t ncache_, int64_t c0, int64_t c1_,
+    __host__ __device__ void init(const int64_t* us_, const int64_t* us_s_, int64_t ncache_, int64_t c0, int64_t c1_,
                          int64_t u0, int N_, int pm) {
         us = us_; us_s = us_s_; base = u0; ncache = ncache_;
         c = c0; c1 = c1_; u = u0; N = N_; partial = pm; prev_group = -1;
         ubeg = at(u);
         uend = at(u + 1);
     }
-    __device__ int64_t at(int64_t v) const { return (v - base < ncache) ? us_s[v - base] : us[v]; }
+    __host__ __device__ int64_t at(int64_t v) const { return (v - base < ncache) ? us_s[v - base] : us[v]; }
     // merge group of unit uu (units are (b * Hkv + kvh) * N + r, far below 2^31)
-    __device__ int64_t group_of(int64_t uu) const { return partial ? uu : (int64_t)((uint32_t)uu / (uint32_t)N); }
-    __device__ bool next(Tile& t) {
+    __host__ __device__ int64_t group_of(int64_t uu) const { return partial ? uu : (int64_t)((uint32_t)uu / (uint32_t)N); }
+    __host__ __device__ bool next(Tile& t) {
         if (c >= c1) return false;
         while (uend <= c) {
             ++u;
@@ -95,7 +96,7 @@ struct Ring {
 
 // First unit whose chunk range contains chunk c0 (binary search over the
 // unit prefix us[0..U]).
-__device__ __forceinline__ int64_t unit_of_chunk(const int64_t* us, int64_t U, int64_t c0) {
+__host__ __device__ __forceinline__ int64_t unit_of_chunk(const int64_t* us, int64_t U, int64_t c0) {
     int64_t lo = 0, hi = U - 1;
     while (lo < hi) {
         const int64_t mid = (lo + hi + 1) >> 1;

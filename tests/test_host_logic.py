@@ -6,11 +6,18 @@ partial slot per worker that touches it.  These tests check the arithmetic the
 planner and kernels share (worker_of / worker_begin in dcp_internal.cuh): every
 worker in play owns at least one chunk, worker_of inverts the ranges, and the
 segment count of a group equals the number of distinct workers touching it,
-including when there are fewer chunks than workers.
+including when there are fewer chunks than workers.  The last test runs the
+header code itself (compiled as host code) over random unit layouts.
 """
+
+import os
+import shutil
+import subprocess
 
 import numpy as np
 import pytest
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 def worker_begin(w, W, P):
@@ -54,3 +61,18 @@ def test_segment_counts_match_distinct_workers():
             assert cnt == len(owners)
             total += cnt
         assert total <= We + len(groups)
+
+
+def test_tile_walk_and_worker_ranges_on_the_header_code(tmp_path):
+    """The header code itself (worker ranges, unit lookup, the MLA kernels'
+    tile walk), compiled by nvcc as host code and run on random unit layouts
+    (tests/host/tile_walk_check.cu states the properties checked)."""
+    nvcc = os.environ.get("NVCC") or shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = str(tmp_path / "tile_walk_check")
+    src = os.path.join(_HERE, "host", "tile_walk_check.cu")
+    r = subprocess.run([nvcc, "-std=c++17", "-O1", "-x", "cu", src, "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
