@@ -76,3 +76,46 @@ def test_tile_walk_and_worker_ranges_on_the_header_code(tmp_path):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
+def test_closed_forms_of_the_cuda_path_match_the_oracle(tmp_path):
+    """owner_rank / local_pos / local_len / local_len32 of dcp_internal.cuh,
+    compiled as host code (tests/host/closed_forms_dump.cu), against the
+    oracle bit-exactly where the oracle's brute-force count finishes quickly
+    (the local position of token t is the count of its rank's tokens before
+    it); at every size, the local lengths partition L with a spread <= I and
+    the 32-bit form equals the 64-bit one."""
+    import oracle
+    nvcc = os.environ.get("NVCC") or shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = str(tmp_path / "closed_forms_dump")
+    src = os.path.join(_HERE, "host", "closed_forms_dump.cu")
+    r = subprocess.run([nvcc, "-std=c++17", "-O1", "-x", "cu", src, "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=60).stdout.split("\n")
+    small = 200000
+    lens = {}
+    n_t = n_l = 0
+    for line in out:
+        f = line.split()
+        if not f:
+            continue
+        if f[0] == "T":
+            N, I, t, owner, lpos = (int(x) for x in f[1:])
+            assert owner == oracle.rank_of(t, N, I), line
+            if t < small:
+                assert lpos == oracle.local_len(t, owner, N, I), line
+            n_t += 1
+        else:
+            N, I, L, rr, l64, l32 = (int(x) for x in f[1:])
+            if L < small:
+                assert l64 == oracle.local_len(L, rr, N, I), line
+            if l32 >= 0:
+                assert l32 == l64, line
+            lens.setdefault((N, I, L), {})[rr] = l64  # (the case list repeats some L)
+            n_l += 1
+    assert n_t > 300 and n_l > 300
+    for (N, I, L), by_rank in lens.items():
+        v = [by_rank[r] for r in range(N)]
+        assert sum(v) == L and max(v) - min(v) <= I, (N, I, L, v)
