@@ -130,3 +130,83 @@ def test_each_workload_selects_its_kernel(libdcp, name, kernel):
     from context_decode_attention_gb300 import dcp_attention_kernel, params_from_config
     from dcp_workloads import config
     assert dcp_attention_kernel(params_from_config(config(name), kv_scale=0.01 if "fp8" in name else 1.0)) == kernel
+
+
+# ----- host validation of the entry points beyond decode (no GPU is touched:
+# every call below returns before its first CUDA call)
+
+def _mla(name="mla_fp8_mixed", **kw):
+    from context_decode_attention_gb300 import params_from_config
+    from dcp_workloads import config
+    return params_from_config(config(name, **kw))
+
+
+def test_sparse_workspace_size_rules(libdcp):
+    """Argument rules of the size query (the size itself needs the device's SM
+    count: tests/test_gpu_sparse.py checks it)."""
+    p = _mla()
+    n = ctypes.c_size_t(0)
+    assert libdcp.dcp_sparse_workspace_size(ctypes.byref(p), 4, 0, ctypes.byref(n)) == 1
+    assert libdcp.dcp_sparse_workspace_size(ctypes.byref(p), -1, 64, ctypes.byref(n)) == 1
+    g = _good()  # GQA: the sparse path is MLA only
+    assert libdcp.dcp_sparse_workspace_size(ctypes.byref(g), 4, 64, ctypes.byref(n)) == 2
+    wide = _mla(N=33)
+    assert libdcp.dcp_sparse_workspace_size(ctypes.byref(wide), 4, 64, ctypes.byref(n)) == 2
+
+
+def test_sparse_entry_points_validate_before_launching(libdcp):
+    p = _mla()
+    dummy = ctypes.c_void_p(256)
+    # empty batch: nothing to do
+    assert libdcp.dcp_sparse_decode_attention(ctypes.byref(p), 0, 64, dummy, dummy, dummy, 10, dummy, 4, dummy,
+                                              dummy, None, dummy, 1 << 20, None) == 0
+    # missing query / candidates / output
+    for i in (3, 4, 10):
+        args = [ctypes.byref(p), 2, 64, dummy, dummy, dummy, 10, dummy, 4, dummy, dummy, None, dummy, 1 << 30, None]
+        args[i] = None
+        assert libdcp.dcp_sparse_decode_attention(*args) == 1, i
+    # no workspace
+    assert libdcp.dcp_sparse_decode_attention(ctypes.byref(p), 2, 64, dummy, dummy, dummy, 10, dummy, 4, dummy,
+                                              dummy, None, None, 0, None) == 4
+    assert libdcp.dcp_sparse_localize(ctypes.byref(p), 2, 0, dummy, dummy, dummy, dummy, dummy, 1 << 20,
+                                      None) == 1
+
+
+def test_pcp_partition_and_prefill_rules(libdcp):
+    dummy = ctypes.c_void_p(256)
+    # K >= 1, B >= 0, max_q >= 0; a workspace for the error word; empty batch is a no-op
+    assert libdcp.dcp_pcp_partition(0, 2, dummy, dummy, 8, dummy, dummy, dummy, 256, None) == 1
+    assert libdcp.dcp_pcp_partition(2, -1, dummy, dummy, 8, dummy, dummy, dummy, 256, None) == 1
+    assert libdcp.dcp_pcp_partition(2, 2, dummy, dummy, 8, dummy, dummy, None, 0, None) == 4
+    assert libdcp.dcp_pcp_partition(2, 0, None, None, 8, None, None, dummy, 256, None) == 0
+    assert libdcp.dcp_pcp_partition(2, 2, dummy, None, 8, dummy, dummy, dummy, 256, None) == 1
+    g = _good()
+    args = [ctypes.byref(g), 0, 16, dummy, dummy, dummy, dummy, 10, dummy, 4, dummy, dummy, dummy, dummy,
+            None, None, dummy, 256, None]
+    assert libdcp.dcp_prefill_attention(*args) == 0  # empty batch
+    args[1] = -1
+    assert libdcp.dcp_prefill_attention(*args) == 1
+    args[1] = 2
+    args[3] = None  # no query
+    assert libdcp.dcp_prefill_attention(*args) == 1
+    args[3] = dummy
+    args[16], args[17] = None, 0
+    assert libdcp.dcp_prefill_attention(*args) == 4
+    m = _mla()  # MLA prefill is not built
+    args = [ctypes.byref(m), 2, 16, dummy, dummy, dummy, dummy, 10, dummy, 4, dummy, dummy, dummy, dummy,
+            None, None, dummy, 256, None]
+    assert libdcp.dcp_prefill_attention(*args) == 2
+
+
+def test_transfer_blocks_rules(libdcp):
+    p = _good()
+    dummy = ctypes.c_void_p(256)
+    # B < 0; no workspace; empty batch with no totals is a no-op; missing inputs
+    assert libdcp.dcp_transfer_blocks(ctypes.byref(p), -1, dummy, dummy, 4, 10, dummy, dummy, dummy, None,
+                                      dummy, 256, None) == 1
+    assert libdcp.dcp_transfer_blocks(ctypes.byref(p), 2, dummy, dummy, 4, 10, dummy, dummy, dummy, None,
+                                      None, 0, None) == 4
+    assert libdcp.dcp_transfer_blocks(ctypes.byref(p), 0, None, None, 4, 10, None, None, None, None,
+                                      dummy, 256, None) == 0
+    assert libdcp.dcp_transfer_blocks(ctypes.byref(p), 2, None, dummy, 4, 10, dummy, dummy, dummy, None,
+                                      dummy, 256, None) == 1

@@ -105,3 +105,24 @@ def test_sparse_candidate_past_position_is_reported():
     ref_o, _ = oracle.sparse_attention(wl, np.where(bad >= int(wl.seq_lens[0]), -1, bad))
     Hq = int(wl.cfg["Hq"])
     assert np.abs(f64(out).reshape(ref_o.shape)[:Hq] - ref_o[:Hq]).max() <= tol_for(wl.cfg)[0]
+
+
+def test_sparse_workspace_size_grows_with_batch_and_k():
+    """The size query on the device: the staging area alone holds every rank's
+    copy of every row's k candidates (k rounded up to 64 tokens); a smaller
+    workspace is refused before any work is enqueued."""
+    import ctypes
+    import context_decode_attention_gb300 as dcp
+    lib = dcp.lib()
+    p = dcp.params_from_config(config("mla_fp8_mixed"))
+    sizes = {}
+    for B, k in [(0, 64), (1, 64), (4, 64), (4, 100), (4, 2048), (16, 2048)]:
+        sizes[(B, k)] = dcp.dcp_sparse_workspace_size(p, B, k)
+    assert sizes[(1, 64)] < sizes[(4, 64)] < sizes[(16, 2048)]
+    assert sizes[(4, 64)] < sizes[(4, 100)] <= sizes[(4, 2048)]
+    assert sizes[(16, 2048)] >= p.N * 16 * p.Tq * 2048 * 576
+    small = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    dummy = ctypes.c_void_p(small.data_ptr())
+    rc = lib.dcp_sparse_decode_attention(ctypes.byref(p), 2, 64, dummy, dummy, dummy, 10, dummy, 4, dummy, dummy,
+                                         None, dummy, 1024, None)
+    assert rc == 4
