@@ -44,7 +44,16 @@ def params_from_config(cfg, kv_scale=1.0):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device address of a tensor argument.  The library reads and writes
+    through plain pointers, so a host tensor or a strided view would be read
+    as something else: both are refused here, before any call."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"libdcp takes device tensors; got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"libdcp takes contiguous tensors; got strides {tuple(t.stride())} for shape {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):

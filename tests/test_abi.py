@@ -210,3 +210,18 @@ def test_transfer_blocks_rules(libdcp):
                                       dummy, 256, None) == 0
     assert libdcp.dcp_transfer_blocks(ctypes.byref(p), 2, None, dummy, 4, 10, dummy, dummy, dummy, None,
                                       dummy, 256, None) == 1
+
+
+def test_binding_refuses_host_tensors(libdcp):
+    """The Python binding passes plain pointers, so it refuses a host tensor
+    before calling into the library (no GPU is touched)."""
+    import torch
+    import context_decode_attention_gb300 as dcp
+    o = torch.zeros((2, 3, 8))
+    l = torch.zeros((2, 3))
+    with pytest.raises(ValueError, match="device tensors"):
+        dcp.dcp_lse_merge(2, 3, 8, o, l, torch.zeros((3, 8)), dcp.DCP_F32, torch.zeros(3))
+    with pytest.raises(ValueError, match="device tensors"):
+        dcp.dcp_pcp_partition(2, torch.zeros(2, dtype=torch.int32), torch.zeros(2, dtype=torch.int32), 8,
+                              torch.zeros((2, 8), dtype=torch.int32), torch.zeros(2, dtype=torch.int32),
+                              workspace=torch.zeros(256, dtype=torch.uint8))
