@@ -77,7 +77,9 @@ extern "C" {
 #define DCP_DEV_ERR_TOKEN 0x2u      /* a token's request or position lies outside its request */
 #define DCP_DEV_ERR_TABLE 0x4u      /* a rank needs more blocks than max_blocks */
 #define DCP_DEV_ERR_STALE 0x8u      /* local_lens disagree with seq_lens under (N, I) */
-#define DCP_DEV_ERR_TIMEOUT 0x10u   /* a bounded wait inside a kernel gave up */
+#define DCP_DEV_ERR_TIMEOUT 0x10u   /* a bounded wait inside a kernel gave up (or a tensor-core
+                                       kernel found its shared memory off the 1024-byte boundary
+                                       its swizzled layouts need, and did nothing) */
 #define DCP_DEV_ERR_ROWS 0x20u      /* a request's padded prefill rows exceed the row capacity */
 
 typedef enum { DCP_F32 = 0, DCP_BF16 = 1, DCP_FP8_E4M3 = 2 } dcp_dtype;
