@@ -8,7 +8,7 @@ back to the CPU: if the library is missing or cannot load, every call raises.
 Functions carry the C ABI's names (include/dcp.h):
   dcp_workspace_size, dcp_workspace_init, dcp_get_error, dcp_slot_mapping, dcp_transfer_blocks, dcp_pcp_partition, dcp_prefill_attention,
   dcp_sparse_workspace_size, dcp_sparse_localize, dcp_sparse_decode_attention,
-  dcp_partial_attention, dcp_lse_merge, dcp_decode_attention
+  dcp_partial_attention, dcp_lse_merge, dcp_decode_attention, dcp_decode_attention_noalloc
 """
 
 import ctypes
