@@ -1,7 +1,8 @@
 // DCP-localised sparse (top-k) attention: candidate localisation and the
 // staging of every rank's candidates for the dense decode kernels.
 //
-// "GLM-5.3 Optimizations, Part 2": sparse MLA attends to a selected set of
+// The GLM-5.3 context-parallelism page (vLLM's second GLM-5.3 article),
+// "What DP and TP leave unresolved": sparse MLA attends to a selected set of
 // 2,048 tokens per query, chosen by an indexer.  "vLLM DCP and PCP" (its
 // source-and-test table): under DCP the candidates are localised, i.e. each
 // rank keeps those it owns, at their local positions, and the exact result is

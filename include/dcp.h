@@ -256,8 +256,8 @@ int dcp_prefill_attention(const dcp_params* params, int32_t B, int32_t Tq, const
                           size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * DCP-localised sparse (top-k) attention, MLA layout ("GLM-5.3 Optimizations,
- * Part 2": sparse MLA attends to a selected set of 2,048 tokens per query,
+ * DCP-localised sparse (top-k) attention, MLA layout (the GLM-5.3
+ * context-parallelism page, "What DP and TP leave unresolved": sparse MLA attends to a selected set of 2,048 tokens per query,
  * chosen by an indexer; "vLLM DCP and PCP", its source-and-test table: under
  * DCP the candidates are localised to the ranks that own them, and the exact
  * result is the LSE merge of the ranks' partials).

@@ -182,8 +182,9 @@ def merge(o_parts, lse_parts):
 
 def sparse_localize(cand, N, I, seq_lens, Tq):
     """Candidate localization under DCP ("vLLM DCP and PCP", the indexer
-    localisation tests in its source-and-test table; "GLM-5.3 ... Part 2":
-    sparse MLA attends to a selected token set).  For every query row's
+    localisation tests in its source-and-test table; the GLM-5.3
+    context-parallelism page, "What DP and TP leave unresolved": sparse MLA
+    attends to a selected token set).  For every query row's
     candidate list (global positions, -1 unused), each rank's candidates in
     list order, as its local positions (ownership by the rank equation, local
     positions by the running count of local_layout).  Returns (local [N, rows,
