@@ -14,17 +14,19 @@ void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order
 
 namespace {
 
+// SM count of the current device, cached per device.  Host threads may call
+// in concurrently; they all store the same value, through an atomic.
 int device_sms() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (dev < 0 || dev >= 64) return 0;
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 bool valid_dtype(int d, bool allow_fp8) {
