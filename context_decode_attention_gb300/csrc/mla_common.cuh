@@ -3,6 +3,8 @@
 // ring-slot counter and the 2D tensor-map encoder.
 #pragma once
 
+#include <atomic>
+
 #include <cudaTypedefs.h>
 
 #include "dcp_internal.cuh"
@@ -105,17 +107,22 @@ __host__ __device__ __forceinline__ int64_t unit_of_chunk(const int64_t* us, int
     return lo;
 }
 
+// The driver's tensor-map encoder, looked up on first use (through an atomic:
+// host threads may call in concurrently; a failed lookup is retried).
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+    if (!f) {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+            q == cudaDriverEntryPointSuccess) {
+            f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+            fn.store(f, std::memory_order_release);
+        }
     }
-    return fn;
+    return f;
 }
 
 // Row-major [rows x cols] tensor with a row pitch of row_bytes; boxes of
