@@ -47,9 +47,13 @@ def build(force=False, verbose=False, extra=()):
         return LIB
     os.makedirs(OUT, exist_ok=True)
     srcs = _sources()
+    # objects in a directory of this process's own, so that builds running at
+    # the same time (test workers, say) never link each other's half-written objects
+    objdir = os.path.join(OUT, f"obj.{os.getpid()}")
+    os.makedirs(objdir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -58,12 +62,15 @@ def build(force=False, verbose=False, extra=()):
             print(r.stdout + r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(compile_one, srcs))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-           "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
+    try:
+        with cf.ThreadPoolExecutor(max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
+            objs = list(ex.map(compile_one, srcs))
+        cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+               "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+    finally:
+        shutil.rmtree(objdir, ignore_errors=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
