@@ -793,6 +793,7 @@ def main():
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
 
     total_ms, attn_ms, write_ms = reduce_max([total_ms, attn_ms, write_ms], world)
+    write_bytes = sum(t.numel() * t.element_size() for t in (dw.new_k, dw.new_v) if t is not None)
     ms_per_step = total_ms / K
     tokens_per_step = int(cfg["B"]) * int(cfg["Tq"])
     value = world * tokens_per_step / (ms_per_step / 1e3)
@@ -827,6 +828,9 @@ def main():
         "config": workload_config(cfg, wl, l2=l2_note),
         "kv_read_tbps": alg["kv_bytes"] / t_attn / 1e12,
         "cache_write_ms": write_ms,
+        # the step's new K/V rows scattered into the paged cache (slot mapping + write)
+        "cache_write_bytes": int(write_bytes),
+        "cache_write_gbps": write_bytes / (write_ms / 1e3) / 1e9,
         "roofline": roof,
         "gpu_launches": int(launches),
         "clocks": clk,
