@@ -522,3 +522,15 @@ def test_sparse_localize_matches_closed_form(N, I):
             mine = c[(c // I) % N == r]
             assert np.array_equal(local[r, i, :counts[r, i]], (mine // (N * I)) * I + mine % I)
             assert np.all(local[r, i, counts[r, i]:] == -1)
+
+
+def test_one_million_tokens_on_dcp8_store_an_eighth_each():
+    for ln in _read("capacity_1m_dcp8.txt"):
+        shard, gib = ln.split("|")
+        L, N, I, each = map(int, shard.split())
+        total_gib, per_gpu_gib = map(float, gib.split())
+        lens = [oracle.local_len(L, r, N, I) for r in range(N)]
+        assert lens == [each] * N and sum(lens) == L
+        # every rank keeps the same share of the request's KV bytes: the page's
+        # per-GPU figure is its total over N, to its rounding of 0.1 GiB
+        assert abs(total_gib * max(lens) / L - per_gpu_gib) <= 0.05
