@@ -102,12 +102,71 @@ def _nbytes(t):
     return 0 if t is None else t.numel() * t.element_size()
 
 
+# Bytes per element of each dcp_dtype.
+_ESIZE = {DCP_F32: 4, DCP_BF16: 2, DCP_FP8_E4M3: 1}
+
+
+def _need(t, name, nbytes, itemsize):
+    """Refuse a buffer with the wrong element size or fewer bytes than the call
+    reads or writes through it: the library sees only the address, so a short
+    buffer would be read past its end on the device."""
+    if t is None:
+        return
+    if t.element_size() != itemsize:
+        raise ValueError(f"{name}: expected {itemsize}-byte elements, got {t.dtype}")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name}: has {have} bytes; these params and sizes need {nbytes}")
+
+
+def _kv_row(params):
+    """Key and value elements per token row of the pools: (GQA) Hkv x D, (MLA) Dk and none."""
+    if params.layout == DCP_LAYOUT_MLA:
+        return params.Dk, 0
+    return params.Hkv * params.Dk, params.Hkv * params.Dv
+
+
+def _need_pools(params, k_pool, v_pool, num_blocks):
+    kv = _ESIZE.get(params.kv_dtype, 1)
+    row_k, row_v = _kv_row(params)
+    slots = int(num_blocks) * params.block_size
+    _need(k_pool, "k_pool", slots * row_k * kv, kv)
+    if row_v:
+        _need(v_pool, "v_pool", slots * row_v * kv, kv)
+
+
+def _need_attention(params, B, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens):
+    """Sizes of the inputs every attention entry point reads (layouts in include/dcp.h)."""
+    rows = B * params.Tq * params.Hq
+    _need(q, "q", rows * params.Dk * _ESIZE.get(params.q_dtype, 1), _ESIZE.get(params.q_dtype, 1))
+    _need_pools(params, k_pool, v_pool, num_blocks)
+    _need(block_tables, "block_tables", params.N * B * int(block_tables.shape[-1]) * 4, 4)
+    _need(seq_lens, "seq_lens", B * 4, 4)
+    _need(local_lens, "local_lens", params.N * B * 4, 4)
+    return rows
+
+
 def dcp_slot_mapping(params, seq_lens, tok_req=None, tok_pos=None, block_tables=None, num_blocks=0,
                      owner=None, slots=None, local_lens=None, virt_blocks=None, rank_blocks=None,
                      new_k=None, new_v=None, k_pool=None, v_pool=None, workspace=None, stream=None):
     B = int(seq_lens.numel())
     T = 0 if tok_req is None else int(tok_req.numel())
     max_blocks = 0 if block_tables is None else int(block_tables.shape[-1])
+    N = params.N
+    _need(seq_lens, "seq_lens", B * 4, 4)
+    _need(tok_req, "tok_req", T * 4, 4)
+    _need(tok_pos, "tok_pos", T * 8, 8)
+    _need(block_tables, "block_tables", N * B * max_blocks * 4, 4)
+    _need(owner, "owner", T, 1)
+    _need(slots, "slots", N * T * 8, 8)
+    _need(local_lens, "local_lens", N * B * 4, 4)
+    _need(virt_blocks, "virt_blocks", B * 4, 4)
+    _need(rank_blocks, "rank_blocks", N * B * 4, 4)
+    kv = _ESIZE.get(params.kv_dtype, 1)
+    row_k, row_v = _kv_row(params)
+    _need(new_k, "new_k", T * row_k * kv, kv)
+    _need(new_v, "new_v", T * row_v * kv, kv)
+    _need_pools(params, k_pool, v_pool, num_blocks)
     _check(lib().dcp_slot_mapping(ctypes.byref(params), B, _ptr(seq_lens), T, _ptr(tok_req), _ptr(tok_pos),
                                   _ptr(block_tables), max_blocks, int(num_blocks), _ptr(owner), _ptr(slots),
                                   _ptr(local_lens), _ptr(virt_blocks), _ptr(rank_blocks), _ptr(new_k),
@@ -171,6 +230,10 @@ def dcp_sparse_decode_attention(params, q, cand, k_pool, num_blocks, block_table
 
 def dcp_partial_attention(params, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens,
                           out_partial, lse_partial, workspace, stream=None):
+    B = int(seq_lens.numel())
+    rows = _need_attention(params, B, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens)
+    _need(out_partial, "out_partial", params.N * rows * params.Dv * 4, 4)
+    _need(lse_partial, "lse_partial", params.N * rows * 4, 4)
     _check(lib().dcp_partial_attention(ctypes.byref(params), int(seq_lens.numel()), _ptr(q), _ptr(k_pool),
                                        _ptr(v_pool), int(num_blocks), _ptr(block_tables),
                                        int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(local_lens),
@@ -178,8 +241,16 @@ def dcp_partial_attention(params, q, k_pool, v_pool, num_blocks, block_tables, s
                                        _nbytes(workspace), _stream(stream)), "dcp_partial_attention")
 
 
+def _need_decode_out(params, rows, out, lse):
+    _need(out, "out", rows * params.Dv * _ESIZE.get(params.out_dtype, 1), _ESIZE.get(params.out_dtype, 1))
+    _need(lse, "lse", rows * 4, 4)
+
+
 def dcp_decode_attention(params, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens,
                          out, lse, workspace, stream=None):
+    B = int(seq_lens.numel())
+    rows = _need_attention(params, B, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens)
+    _need_decode_out(params, rows, out, lse)
     _check(lib().dcp_decode_attention(ctypes.byref(params), int(seq_lens.numel()), _ptr(q), _ptr(k_pool),
                                       _ptr(v_pool), int(num_blocks), _ptr(block_tables),
                                       int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(local_lens),
@@ -188,6 +259,11 @@ def dcp_decode_attention(params, q, k_pool, v_pool, num_blocks, block_tables, se
 
 
 def dcp_lse_merge(N, rows, Dv, out_partial, lse_partial, out, out_dtype, lse=None, stream=None):
+    n = max(0, int(N)) * max(0, int(rows))
+    _need(out_partial, "out_partial", n * int(Dv) * 4, 4)
+    _need(lse_partial, "lse_partial", n * 4, 4)
+    _need(out, "out", max(0, int(rows)) * int(Dv) * _ESIZE.get(int(out_dtype), 1), _ESIZE.get(int(out_dtype), 1))
+    _need(lse, "lse", max(0, int(rows)) * 4, 4)
     _check(lib().dcp_lse_merge(int(N), int(rows), int(Dv), _ptr(out_partial), _ptr(lse_partial), _ptr(out),
                                int(out_dtype), _ptr(lse), _stream(stream)), "dcp_lse_merge")
 
@@ -199,6 +275,9 @@ def dcp_decode_attention_noalloc(params, q, k_pool, v_pool, num_blocks, block_ta
     For callers that cannot allocate device memory; calls must not overlap on
     the GPU (they share one scratch buffer).  See include/dcp.h.
     """
+    B = int(seq_lens.numel())
+    rows = _need_attention(params, B, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens)
+    _need_decode_out(params, rows, out, lse)
     _check(lib().dcp_decode_attention_noalloc(ctypes.byref(params), int(seq_lens.numel()), _ptr(q), _ptr(k_pool),
                                               _ptr(v_pool), int(num_blocks), _ptr(block_tables),
                                               int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(local_lens),

@@ -225,3 +225,63 @@ def test_binding_refuses_host_tensors(libdcp):
         dcp.dcp_pcp_partition(2, torch.zeros(2, dtype=torch.int32), torch.zeros(2, dtype=torch.int32), 8,
                               torch.zeros((2, 8), dtype=torch.int32), torch.zeros(2, dtype=torch.int32),
                               workspace=torch.zeros(256, dtype=torch.uint8))
+
+
+def test_binding_refuses_buffers_too_small_for_the_params(libdcp):
+    """The library reads through plain pointers, so a short buffer or one of
+    the wrong element size would be read past its end on the device.  The
+    binding compares every buffer with the params and sizes before calling in
+    (checked here on host tensors: the size check comes first)."""
+    import torch
+    import context_decode_attention_gb300 as dcp
+    from dcp_workloads import config
+
+    cfg = config("gqa_llama8b", B=2)
+    p = dcp.params_from_config(cfg)
+    B, Tq, Hq, Hkv, D, N, bs, nb, mb = 2, 1, 32, 8, 128, 4, 16, 10, 3
+    ok = dict(
+        q=torch.zeros((B, Tq, Hq, D), dtype=torch.bfloat16),
+        k_pool=torch.zeros((nb, Hkv, bs, D), dtype=torch.bfloat16),
+        v_pool=torch.zeros((nb, Hkv, bs, D), dtype=torch.bfloat16),
+        block_tables=torch.zeros((N, B, mb), dtype=torch.int32),
+        seq_lens=torch.zeros(B, dtype=torch.int32), local_lens=torch.zeros((N, B), dtype=torch.int32),
+        out=torch.zeros((B, Tq, Hq, D), dtype=torch.bfloat16), lse=torch.zeros((B, Tq, Hq)),
+    )
+
+    def decode(**over):
+        a = dict(ok, **over)
+        dcp.dcp_decode_attention(p, a["q"], a["k_pool"], a["v_pool"], nb, a["block_tables"], a["seq_lens"],
+                                 a["local_lens"], a["out"], a["lse"], torch.zeros(256, dtype=torch.uint8))
+
+    # right sizes: the checks pass and the host-tensor refusal follows
+    with pytest.raises(ValueError, match="device tensors"):
+        decode()
+    bad = {
+        "q": ok["q"][:1],                                             # one request short
+        "k_pool": ok["k_pool"][:-1],                                  # one block short
+        "v_pool": ok["v_pool"].to(torch.float32),                     # 4-byte elements for a bf16 cache
+        "block_tables": ok["block_tables"].to(torch.int64),
+        "local_lens": ok["local_lens"][:1],
+        "out": ok["out"].to(torch.float32)[..., :64],                 # f32 where the params say bf16
+        "lse": ok["lse"][:1],
+    }
+    for name, t in bad.items():
+        with pytest.raises(ValueError, match=name):
+            decode(**{name: t.contiguous()})
+
+    # the merge: N partials of rows x Dv
+    o, l = torch.zeros((2, 3, 8)), torch.zeros((2, 3))
+    with pytest.raises(ValueError, match="out_partial"):
+        dcp.dcp_lse_merge(2, 3, 8, o[:1].contiguous(), l, torch.zeros((3, 8)), dcp.DCP_F32, torch.zeros(3))
+    with pytest.raises(ValueError, match="out"):
+        dcp.dcp_lse_merge(2, 3, 8, o, l, torch.zeros((3, 8), dtype=torch.bfloat16), dcp.DCP_F32, torch.zeros(3))
+
+    # slot mapping: slots are int64 [N][T]
+    T = 5
+    with pytest.raises(ValueError, match="slots"):
+        dcp.dcp_slot_mapping(p, ok["seq_lens"], torch.zeros(T, dtype=torch.int32), torch.zeros(T, dtype=torch.int64),
+                             ok["block_tables"], nb, slots=torch.zeros((N, T), dtype=torch.int32))
+    with pytest.raises(ValueError, match="new_k"):
+        dcp.dcp_slot_mapping(p, ok["seq_lens"], torch.zeros(T, dtype=torch.int32), torch.zeros(T, dtype=torch.int64),
+                             ok["block_tables"], nb, new_k=torch.zeros((T - 1, Hkv, D), dtype=torch.bfloat16),
+                             k_pool=ok["k_pool"], v_pool=ok["v_pool"])
