@@ -178,6 +178,13 @@ def dcp_transfer_blocks(params, seq_lens, block_tables, num_blocks, counts, bloc
                         totals=None, workspace=None, stream=None):
     """Per-rank non-empty blocks of each request with their token counts (and
     the batch's slots / tokens moved in totals[2]); see include/dcp.h."""
+    B, M, N = int(seq_lens.numel()), int(block_tables.shape[-1]), params.N
+    _need(seq_lens, "seq_lens", B * 4, 4)
+    _need(block_tables, "block_tables", N * B * M * 4, 4)
+    _need(counts, "counts", N * B * 4, 4)
+    _need(blocks, "blocks", N * B * M * 4, 4)
+    _need(fills, "fills", N * B * M * 4, 4)
+    _need(totals, "totals", 2 * 8, 8)
     _check(lib().dcp_transfer_blocks(ctypes.byref(params), int(seq_lens.numel()), _ptr(seq_lens),
                                      _ptr(block_tables), int(block_tables.shape[-1]), int(num_blocks),
                                      _ptr(counts), _ptr(blocks), _ptr(fills), _ptr(totals), _ptr(workspace),
@@ -187,6 +194,11 @@ def dcp_transfer_blocks(params, seq_lens, block_tables, num_blocks, counts, bloc
 def dcp_pcp_partition(K, ctx_lens, q_lens, max_q, pos, padded_lens, workspace=None, stream=None):
     """Head-tail prefill partition over K PCP ranks into pos [B, max_q] (gathered
     order, -1 = padding) and padded_lens [B]; see include/dcp.h."""
+    B = int(ctx_lens.numel())
+    _need(ctx_lens, "ctx_lens", B * 4, 4)
+    _need(q_lens, "q_lens", B * 4, 4)
+    _need(pos, "pos", B * max(0, int(max_q)) * 4, 4)
+    _need(padded_lens, "padded_lens", B * 4, 4)
     _check(lib().dcp_pcp_partition(int(K), int(ctx_lens.numel()), _ptr(ctx_lens), _ptr(q_lens), int(max_q),
                                    _ptr(pos), _ptr(padded_lens), _ptr(workspace), _nbytes(workspace),
                                    _stream(stream)), "dcp_pcp_partition")
@@ -197,6 +209,19 @@ def dcp_prefill_attention(params, q, q_pos, k_pool, v_pool, num_blocks, block_ta
     """Causal prefill of gathered query rows q [B, Tq, Hq, D] at positions
     q_pos [B, Tq]: per-rank partials, and the merged output when `out` is
     given; see include/dcp.h."""
+    B, Tq, N = int(q.shape[0]), int(q.shape[1]), params.N
+    rows = B * Tq * params.Hq
+    qs, os_ = _ESIZE.get(params.q_dtype, 1), _ESIZE.get(params.out_dtype, 1)
+    _need(q, "q", rows * params.Dk * qs, qs)
+    _need(q_pos, "q_pos", B * Tq * 4, 4)
+    _need_pools(params, k_pool, v_pool, num_blocks)
+    _need(block_tables, "block_tables", N * B * int(block_tables.shape[-1]) * 4, 4)
+    _need(seq_lens, "seq_lens", B * 4, 4)
+    _need(local_lens, "local_lens", N * B * 4, 4)
+    _need(out_partial, "out_partial", N * rows * params.Dv * 4, 4)
+    _need(lse_partial, "lse_partial", N * rows * 4, 4)
+    _need(out, "out", rows * params.Dv * os_, os_)
+    _need(lse, "lse", rows * 4, 4)
     _check(lib().dcp_prefill_attention(ctypes.byref(params), int(q.shape[0]), int(q.shape[1]), _ptr(q), _ptr(q_pos),
                                        _ptr(k_pool), _ptr(v_pool), int(num_blocks), _ptr(block_tables),
                                        int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(local_lens),
@@ -213,6 +238,11 @@ def dcp_sparse_workspace_size(params, B, k):
 
 def dcp_sparse_localize(params, cand, seq_lens, local, counts, workspace=None, stream=None):
     """Each rank's candidates (cand [B*Tq, k]) at their local positions; see include/dcp.h."""
+    R, k, N = int(seq_lens.numel()) * params.Tq, int(cand.shape[-1]), params.N
+    _need(cand, "cand", R * k * 4, 4)
+    _need(seq_lens, "seq_lens", int(seq_lens.numel()) * 4, 4)
+    _need(local, "local", N * R * k * 4, 4)
+    _need(counts, "counts", N * R * 4, 4)
     _check(lib().dcp_sparse_localize(ctypes.byref(params), int(seq_lens.numel()), int(cand.shape[-1]), _ptr(cand),
                                      _ptr(seq_lens), _ptr(local), _ptr(counts), _ptr(workspace), _nbytes(workspace),
                                      _stream(stream)), "dcp_sparse_localize")
@@ -221,6 +251,16 @@ def dcp_sparse_localize(params, cand, seq_lens, local, counts, workspace=None, s
 def dcp_sparse_decode_attention(params, q, cand, k_pool, num_blocks, block_tables, seq_lens, out, lse=None,
                                 workspace=None, stream=None):
     """Attention of every query row over its candidate positions only, DCP-localised; see include/dcp.h."""
+    B, k, N = int(q.shape[0]), int(cand.shape[-1]), params.N
+    rows = B * params.Tq * params.Hq
+    qs, os_ = _ESIZE.get(params.q_dtype, 1), _ESIZE.get(params.out_dtype, 1)
+    _need(q, "q", rows * params.Dk * qs, qs)
+    _need(cand, "cand", B * params.Tq * k * 4, 4)
+    _need_pools(params, k_pool, None, num_blocks)
+    _need(block_tables, "block_tables", N * B * int(block_tables.shape[-1]) * 4, 4)
+    _need(seq_lens, "seq_lens", B * 4, 4)
+    _need(out, "out", rows * params.Dv * os_, os_)
+    _need(lse, "lse", rows * 4, 4)
     _check(lib().dcp_sparse_decode_attention(ctypes.byref(params), int(q.shape[0]), int(cand.shape[-1]), _ptr(q),
                                              _ptr(cand), _ptr(k_pool), int(num_blocks), _ptr(block_tables),
                                              int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(out), _ptr(lse),

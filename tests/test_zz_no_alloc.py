@@ -41,12 +41,18 @@ def test_noalloc_decode_matches_workspace_decode_twice(cfg):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
+    """The C entry point itself turns down a problem whose scratch would not
+    fit in the static buffer (DCP_ERR_WORKSPACE), before it reads any of the
+    argument buffers.  Called through the C ABI directly: the Python binding
+    would already refuse these deliberately tiny stand-in buffers."""
+    import ctypes
     import context_decode_attention_gb300 as dcp
     from context_decode_attention_gb300 import params_from_config
     p = params_from_config(config("mla_bf16_32k"))
     B = 4096  # needs far more partial slots than the static buffer holds
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
     seq = torch.ones(B, dtype=torch.int32, device="cuda")
-    with pytest.raises(dcp.DcpError) as ei:
-        dcp.dcp_decode_attention_noalloc(p, dummy, dummy, None, 1, dummy.view(1, 1, 16), seq, dummy, dummy, None)
-    assert ei.value.code == 4
+    d, s = dummy.data_ptr(), seq.data_ptr()
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = dcp.lib().dcp_decode_attention_noalloc(ctypes.byref(p), B, d, d, None, 1, d, 16, s, d, d, None, stream)
+    assert rc == 4  # DCP_ERR_WORKSPACE
