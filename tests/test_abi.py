@@ -285,3 +285,43 @@ def test_binding_refuses_buffers_too_small_for_the_params(libdcp):
         dcp.dcp_slot_mapping(p, ok["seq_lens"], torch.zeros(T, dtype=torch.int32), torch.zeros(T, dtype=torch.int64),
                              ok["block_tables"], nb, new_k=torch.zeros((T - 1, Hkv, D), dtype=torch.bfloat16),
                              k_pool=ok["k_pool"], v_pool=ok["v_pool"])
+
+
+def test_binding_size_checks_cover_the_other_entry_points(libdcp):
+    """Transfer listing, PCP partition, prefill and sparse calls refuse short
+    buffers on the host too (host tensors: the size check comes first)."""
+    import torch
+    import context_decode_attention_gb300 as dcp
+    from dcp_workloads import config
+
+    i32 = dict(dtype=torch.int32)
+    p = dcp.params_from_config(config("gqa_llama8b", B=2))
+    N, B, M = 4, 2, 3
+    seq, bt = torch.zeros(B, **i32), torch.zeros((N, B, M), **i32)
+    with pytest.raises(ValueError, match="fills"):
+        dcp.dcp_transfer_blocks(p, seq, bt, 10, torch.zeros((N, B), **i32), torch.zeros((N, B, M), **i32),
+                                torch.zeros((N, B, M - 1), **i32), torch.zeros(2, dtype=torch.int64))
+    with pytest.raises(ValueError, match="totals"):
+        dcp.dcp_transfer_blocks(p, seq, bt, 10, torch.zeros((N, B), **i32), totals=torch.zeros(2, **i32))
+    with pytest.raises(ValueError, match="pos"):
+        dcp.dcp_pcp_partition(2, seq, seq, 8, torch.zeros((B, 7), **i32), torch.zeros(B, **i32))
+    with pytest.raises(ValueError, match="device tensors"):  # right sizes: only the host refusal remains
+        dcp.dcp_pcp_partition(2, seq, seq, 8, torch.zeros((B, 8), **i32), torch.zeros(B, **i32))
+
+    Tq, Hq, D = 4, 32, 128
+    pool = torch.zeros((10, 8, 16, D), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="out_partial"):
+        dcp.dcp_prefill_attention(p, torch.zeros((B, Tq, Hq, D), dtype=torch.bfloat16), torch.zeros((B, Tq), **i32),
+                                  pool, pool, 10, bt, seq, torch.zeros((N, B), **i32),
+                                  torch.zeros((N, B, Tq, Hq, D - 1)), torch.zeros((N, B, Tq, Hq)))
+
+    m = dcp.params_from_config(config("mla_fp8_mixed", B=2))
+    k = 64
+    q = torch.zeros((B, 1, 128, 576), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="local"):
+        dcp.dcp_sparse_localize(m, torch.zeros((B, k), **i32), seq, torch.zeros((8, B, k - 1), **i32),
+                                torch.zeros((8, B), **i32))
+    with pytest.raises(ValueError, match="k_pool"):
+        dcp.dcp_sparse_decode_attention(m, q, torch.zeros((B, k), **i32), torch.zeros((10, 64, 575), dtype=torch.uint8),
+                                        10, torch.zeros((8, B, M), **i32), seq,
+                                        torch.zeros((B, 1, 128, 512), dtype=torch.bfloat16))
