@@ -55,12 +55,16 @@ MUTANTS = [
     ("transfer_table_rank_and_request_transposed", C,
      "int32_t id = block_tables[(r * B + b) * max_blocks + k];",
      "int32_t id = block_tables[(b * N + r) * max_blocks + k];"),
+    ("transfer_lists_empty_blocks", C,
+     "if (n == 0) continue;", ";"),
     # PCP head-tail partition
     ("pcp_tail_chunk_not_mirrored", C,
      "const int64_t chunks[2] = {k, 2 * K - 1 - k};", "const int64_t chunks[2] = {k, K + k};"),
     ("pcp_aligns_to_K_not_2K", C,
      "const int64_t aligned = (n + 2 * K - 1) / (2 * K) * (2 * K);",
      "const int64_t aligned = (n + K - 1) / K * K;"),
+    ("pcp_padding_not_marked", C,
+     "row[out++] = rel < n ? (int32_t)(ctx_lens[b] + rel) : -1;", "row[out++] = (int32_t)(ctx_lens[b] + rel);"),
     ("pcp_tail_before_head", C,
      "const int64_t chunks[2] = {k, 2 * K - 1 - k};", "const int64_t chunks[2] = {2 * K - 1 - k, k};"),
     # storage decoding
@@ -92,6 +96,10 @@ MUTANTS = [
      "if (rank >= 0 && orc_rank_of(j, N, I) == rank) continue;"),
     ("query_row_of_wrong_token", C,
      "int64_t t = (id / Hq) % Tq;", "int64_t t = (id / Hq) % Tq; t = Tq - 1 - t;"),
+    ("kv_rows_ignore_request_offset", C,
+     "int64_t row = (req_start[b] + j) * Hkv + kvh;", "int64_t row = j * Hkv + kvh;"),
+    ("lse_in_base_2", C,
+     "double L_row = m + log(sum);", "double L_row = m + log2(sum);"),
     # merge
     ("merge_weight_sign_flipped", C,
      "double a = exp(lse_parts[i * rows + n] - l);", "double a = exp(l - lse_parts[i * rows + n]);"),
