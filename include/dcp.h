@@ -343,8 +343,9 @@ int dcp_decode_attention(const dcp_params* params, int32_t B, const void* q,
  *
  * No passage of the pages has a counterpart to this call: it exists for
  * callers that may not call cudaMalloc (or any allocator) when they run
- * attention -- for example code enqueued while a framework captures a stream,
- * or a plugin inside an engine that owns all device memory.  It computes
+ * attention -- for example a plugin inside an engine that owns all device
+ * memory and hands none out, or code on a path where an allocation's latency
+ * or possible failure is not acceptable.  It computes
  * exactly what dcp_decode_attention computes, with the same arguments minus
  * the workspace: the scratch is a buffer of DCP_STATIC_SCRATCH_BYTES that
  * this library declares as a static device array.  Every device that loads
