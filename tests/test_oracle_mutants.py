@@ -57,7 +57,11 @@ MUTANTS = [
      "int32_t id = block_tables[(b * N + r) * max_blocks + k];"),
     ("transfer_lists_empty_blocks", C,
      "if (n == 0) continue;", ";"),
+    ("transfer_tokens_counted_as_slots", C,
+     "totals[1] += n;", "totals[1] += bs;"),
     # PCP head-tail partition
+    ("pcp_padded_length_left_unpadded", C,
+     "padded_len[b] = (int32_t)aligned;", "padded_len[b] = (int32_t)n;"),
     ("pcp_tail_chunk_not_mirrored", C,
      "const int64_t chunks[2] = {k, 2 * K - 1 - k};", "const int64_t chunks[2] = {k, K + k};"),
     ("pcp_aligns_to_K_not_2K", C,
@@ -75,6 +79,8 @@ MUTANTS = [
     ("fp8_per_tensor_scale_dropped", C,
      "return orc_fp8_e4m3_value(((const uint8_t*)base)[idx]) * scale;",
      "return orc_fp8_e4m3_value(((const uint8_t*)base)[idx]);"),
+    ("fp8_nan_code_dropped", C,
+     "if (e == 0xF && m == 0x7) return NAN;", ";"),
     # attention
     ("causal_bound_off_by_one", C,
      "int64_t g = L - Tq + t + 1;", "int64_t g = L - Tq + t;"),
@@ -101,6 +107,8 @@ MUTANTS = [
     ("lse_in_base_2", C,
      "double L_row = m + log(sum);", "double L_row = m + log2(sum);"),
     # merge
+    ("merge_all_empty_rows_not_special", C,
+     "        if (l == -INFINITY) {\n            lse[n] = -INFINITY;\n            continue;\n        }", ""),
     ("merge_weight_sign_flipped", C,
      "double a = exp(lse_parts[i * rows + n] - l);", "double a = exp(l - lse_parts[i * rows + n]);"),
     ("merge_lse_drops_log_sum", C,
@@ -112,6 +120,10 @@ MUTANTS = [
      "local[r, i, counts[r, i]] = lp[t]", "local[r, i, counts[r, i]] = t"),
     ("sparse_rank_filter_inverted", PY,
      "C = C[layouts[L][0][C] == rank]", "C = C[layouts[L][0][C] != rank]"),
+    ("sparse_query_of_the_first_token", PY,
+     'q = decode(wl.q[b, t], c["q_dtype"])', 'q = decode(wl.q[b, 0], c["q_dtype"])'),
+    ("sparse_rows_without_request_offset", PY,
+     "rows_kv = wl.req_start[b] + C", "rows_kv = C"),
     ("sparse_lse_drops_max_shift", PY,
      "lse[r] = m + np.log(l)", "lse[r] = np.log(l)"),
     ("sparse_output_not_normalised", PY,

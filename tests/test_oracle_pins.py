@@ -534,3 +534,19 @@ def test_one_million_tokens_on_dcp8_store_an_eighth_each():
         # every rank keeps the same share of the request's KV bytes: the page's
         # per-GPU figure is its total over N, to its rounding of 0.1 GiB
         assert abs(total_gib * max(lens) / L - per_gpu_gib) <= 0.05
+
+
+def test_merge_of_only_empty_partials_is_zero_and_minus_inf():
+    """A row no rank holds a token of: its LSE is the log of an empty sum, -inf,
+    and its output is the empty weighted mean, 0 by the empty-shard reading
+    (a rank with no visible token contributes o = 0, L = -inf, weight 0).
+    Rows beside it with one non-empty partial merge to that partial."""
+    rng = np.random.default_rng(5)
+    o = rng.normal(size=(3, 4, 8))
+    lse = np.full((3, 4), -np.inf)
+    lse[1, 2:] = rng.normal(size=2)  # rows 2 and 3: only rank 1 holds tokens
+    o[:, :2] = 0.0                   # empty partials carry zeros
+    out, l = oracle.merge(o, lse)
+    assert np.all(out[:2] == 0) and np.all(np.isneginf(l[:2]))
+    np.testing.assert_allclose(out[2:], o[1, 2:], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(l[2:], lse[1, 2:], rtol=0, atol=1e-15)
