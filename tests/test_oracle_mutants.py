@@ -49,7 +49,12 @@ MUTANTS = [
      "slots[r_own * T + i] = (int64_t)id * bs + lp % bs;", "slots[r_own * T + i] = (int64_t)id * bs + p % bs;"),
     ("block_table_rank_and_request_transposed", C,
      "block_tables[(r_own * B + b) * max_blocks + blk]", "block_tables[(b * N + r_own) * max_blocks + blk]"),
+    ("missing_block_id_not_reported", C,
+     "if (id < 0) { status = -1; continue; }", "if (id < 0) { continue; }"),
     # PD block-transfer listing
+    ("transfer_pool_bound_off_by_one", C,
+     "if (id < 0 || id >= num_blocks) { status = -1; id = -1; }",
+     "if (id < 0 || id > num_blocks) { status = -1; id = -1; }"),
     ("transfer_counts_tokens_as_slots", C,
      "totals[0] += bs;", "totals[0] += n;"),
     ("transfer_table_rank_and_request_transposed", C,
@@ -69,6 +74,8 @@ MUTANTS = [
      "const int64_t aligned = (n + K - 1) / K * K;"),
     ("pcp_padding_not_marked", C,
      "row[out++] = rel < n ? (int32_t)(ctx_lens[b] + rel) : -1;", "row[out++] = (int32_t)(ctx_lens[b] + rel);"),
+    ("pcp_capacity_off_by_one", C,
+     "if (aligned > max_q) {", "if (aligned >= max_q) {"),
     ("pcp_tail_before_head", C,
      "const int64_t chunks[2] = {k, 2 * K - 1 - k};", "const int64_t chunks[2] = {2 * K - 1 - k, k};"),
     # storage decoding
@@ -88,6 +95,9 @@ MUTANTS = [
      "int64_t g = L - Tq + t + 1;", "int64_t g = L;"),
     ("gqa_heads_interleaved_not_grouped", C,
      "int64_t kvh = h / group;", "int64_t kvh = h % Hkv;"),
+    ("keys_without_rope_columns", C,
+     "for (int64_t d = 0; d < Dk; ++d) dot += qv[d] * orc_load(k, row * Dk + d, kv_dtype, kv_scale);",
+     "for (int64_t d = 0; d < Dv; ++d) dot += qv[d] * orc_load(k, row * Dk + d, kv_dtype, kv_scale);"),
     ("softmax_scale_dropped", C,
      "s[cnt] = softmax_scale * dot;", "s[cnt] = dot;"),
     ("lse_drops_max_shift", C,
@@ -107,6 +117,9 @@ MUTANTS = [
     ("lse_in_base_2", C,
      "double L_row = m + log(sum);", "double L_row = m + log2(sum);"),
     # merge
+    ("merge_max_starts_at_zero", C,
+     "        double l = -INFINITY;\n        for (int64_t i = 0; i < N; ++i)",
+     "        double l = 0.0;\n        for (int64_t i = 0; i < N; ++i)"),
     ("merge_all_empty_rows_not_special", C,
      "        if (l == -INFINITY) {\n            lse[n] = -INFINITY;\n            continue;\n        }", ""),
     ("merge_weight_sign_flipped", C,
@@ -124,6 +137,8 @@ MUTANTS = [
      'q = decode(wl.q[b, t], c["q_dtype"])', 'q = decode(wl.q[b, 0], c["q_dtype"])'),
     ("sparse_rows_without_request_offset", PY,
      "rows_kv = wl.req_start[b] + C", "rows_kv = C"),
+    ("sparse_keys_without_rope_columns", PY,
+     "s = scale * (kk[:, g, :] @ q[h])", "s = scale * (kk[:, g, :Dv] @ q[h, :Dv])"),
     ("sparse_lse_drops_max_shift", PY,
      "lse[r] = m + np.log(l)", "lse[r] = np.log(l)"),
     ("sparse_output_not_normalised", PY,

@@ -550,3 +550,30 @@ def test_merge_of_only_empty_partials_is_zero_and_minus_inf():
     assert np.all(out[:2] == 0) and np.all(np.isneginf(l[:2]))
     np.testing.assert_allclose(out[2:], o[1, 2:], rtol=0, atol=1e-15)
     np.testing.assert_allclose(l[2:], lse[1, 2:], rtol=0, atol=1e-15)
+
+
+def test_slot_mapping_reports_a_missing_block():
+    """A token whose local block has no id in its owner's table (-1) gets no
+    slot on any rank and the call reports it; the other tokens are unaffected.
+    N = 2, I = 1, bs = 4, L = 10: rank 0 owns tokens 0, 2, ..., 8 at local
+    positions 0..4, so token 8 is in its second block and token 2 in its first;
+    token 3 is rank 1's local position 1."""
+    seq_lens = np.array([10], dtype=np.int32)
+    tables, _ = _random_tables(2, 1, 4, seq_lens, seed=2)
+    tables[0, 0, 1] = -1
+    sm = oracle.slot_mapping(2, 1, 4, seq_lens, np.array([0, 0, 0], np.int32), np.array([8, 2, 3]), tables)
+    assert sm["status"] == -1
+    assert sm["owner"].tolist() == [0, 0, 1]
+    assert np.all(sm["slots"][:, 0] == -1)
+    assert sm["slots"][:, 1].tolist() == [int(tables[0, 0, 0]) * 4 + 1, -1]
+    assert sm["slots"][:, 2].tolist() == [-1, int(tables[1, 0, 0]) * 4 + 1]
+
+
+def test_transfer_blocks_pool_bound_is_exclusive():
+    """Block ids run from 0 to num_blocks - 1: an id equal to num_blocks is
+    outside the pool and is reported; num_blocks - 1 is not."""
+    for last, bad in ((9, False), (10, True)):
+        tables = np.array([[[7, last]], [[2, 5]]], dtype=np.int32)
+        tb = oracle.transfer_blocks(2, 3, 4, np.array([14]), tables, num_blocks=10)
+        assert (tb["status"] == -1) == bad
+        assert tb["blocks"][0, 0].tolist() == [7, -1 if bad else last]
