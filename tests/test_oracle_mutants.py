@@ -60,6 +60,8 @@ MUTANTS = [
     ("transfer_table_rank_and_request_transposed", C,
      "int32_t id = block_tables[(r * B + b) * max_blocks + k];",
      "int32_t id = block_tables[(b * N + r) * max_blocks + k];"),
+    ("transfer_fill_as_full_block", C,
+     "of[c] = (int32_t)n;", "of[c] = (int32_t)bs;"),
     ("transfer_lists_empty_blocks", C,
      "if (n == 0) continue;", ";"),
     ("transfer_tokens_counted_as_slots", C,
@@ -98,6 +100,8 @@ MUTANTS = [
     ("keys_without_rope_columns", C,
      "for (int64_t d = 0; d < Dk; ++d) dot += qv[d] * orc_load(k, row * Dk + d, kv_dtype, kv_scale);",
      "for (int64_t d = 0; d < Dv; ++d) dot += qv[d] * orc_load(k, row * Dk + d, kv_dtype, kv_scale);"),
+    ("every_head_reads_the_first_heads_query", C,
+     "qv[d] = orc_load(q, id * Dk + d, q_dtype, 1.0);", "qv[d] = orc_load(q, (id - h) * Dk + d, q_dtype, 1.0);"),
     ("softmax_scale_dropped", C,
      "s[cnt] = softmax_scale * dot;", "s[cnt] = dot;"),
     ("lse_drops_max_shift", C,
@@ -124,6 +128,8 @@ MUTANTS = [
      "        if (l == -INFINITY) {\n            lse[n] = -INFINITY;\n            continue;\n        }", ""),
     ("merge_weight_sign_flipped", C,
      "double a = exp(lse_parts[i * rows + n] - l);", "double a = exp(l - lse_parts[i * rows + n]);"),
+    ("merge_partials_indexed_rows_first", C,
+     "o[d] += a * o_parts[(i * rows + n) * Dv + d];", "o[d] += a * o_parts[(n * N + i) * Dv + d];"),
     ("merge_lse_drops_log_sum", C,
      "lse[n] = l + log(asum);", "lse[n] = l;"),
     ("merge_output_not_normalised", C,
@@ -139,6 +145,8 @@ MUTANTS = [
      "rows_kv = wl.req_start[b] + C", "rows_kv = C"),
     ("sparse_keys_without_rope_columns", PY,
      "s = scale * (kk[:, g, :] @ q[h])", "s = scale * (kk[:, g, :Dv] @ q[h, :Dv])"),
+    ("sparse_gqa_heads_interleaved", PY,
+     "g = h // G", "g = h % Hkv"),
     ("sparse_lse_drops_max_shift", PY,
      "lse[r] = m + np.log(l)", "lse[r] = np.log(l)"),
     ("sparse_output_not_normalised", PY,
