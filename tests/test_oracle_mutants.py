@@ -134,7 +134,13 @@ MUTANTS = [
      "lse[n] = l + log(asum);", "lse[n] = l;"),
     ("merge_output_not_normalised", C,
      "for (int64_t d = 0; d < Dv; ++d) o[d] /= asum;", ";"),
+    ("attention_wrapper_swaps_N_and_I", PY,
+     'float(wl.kv_scale), float(c["softmax_scale"]), int(c["N"]), int(c["I"]),',
+     'float(wl.kv_scale), float(c["softmax_scale"]), int(c["I"]), int(c["N"]),'),
     # sparse (top-k) localisation and attention
+    ("sparse_rows_token_major", PY,
+     "            i = b * Tq + t\n            C = cand[i][cand[i] >= 0]",
+     "            i = t * B + b\n            C = cand[i][cand[i] >= 0]"),
     ("sparse_localize_keeps_global_position", PY,
      "local[r, i, counts[r, i]] = lp[t]", "local[r, i, counts[r, i]] = t"),
     ("sparse_rank_filter_inverted", PY,
