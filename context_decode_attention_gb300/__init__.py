@@ -312,8 +312,10 @@ def dcp_decode_attention_noalloc(params, q, k_pool, v_pool, num_blocks, block_ta
                                  out, lse, stream=None):
     """dcp_decode_attention on the library's static scratch (no workspace argument).
 
-    For callers that cannot allocate device memory; calls must not overlap on
-    the GPU (they share one scratch buffer).  See include/dcp.h.
+    For callers that cannot allocate device memory (a plugin in an engine that
+    owns all device memory, or a path that cannot afford an allocation's
+    latency or failure).  Calls must not overlap on the GPU: they share one
+    scratch buffer.  See include/dcp.h.
     """
     B = int(seq_lens.numel())
     rows = _need_attention(params, B, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens)

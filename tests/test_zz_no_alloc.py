@@ -2,8 +2,10 @@
 workspace-taking dcp_decode_attention.
 
 dcp_decode_attention_noalloc serves callers that may not allocate device
-memory while they run attention; its scratch is a static device buffer inside
-the library.  It must give the workspace path's results, call after call,
+memory while they run attention: a plugin inside an engine that owns all
+device memory and hands none out, or a path where an allocation's latency or
+possible failure is not acceptable.  Its scratch is a static device buffer
+inside the library.  It must give the workspace path's results, call after call,
 since every call reuses (and so inherits) the same buffer.  Collected last
 (file name) so a failure here cannot hide another test's result.
 """
