@@ -78,6 +78,8 @@ MUTANTS = [
      "row[out++] = rel < n ? (int32_t)(ctx_lens[b] + rel) : -1;", "row[out++] = (int32_t)(ctx_lens[b] + rel);"),
     ("pcp_capacity_off_by_one", C,
      "if (aligned > max_q) {", "if (aligned >= max_q) {"),
+    ("pcp_positions_without_the_context", C,
+     "row[out++] = rel < n ? (int32_t)(ctx_lens[b] + rel) : -1;", "row[out++] = rel < n ? (int32_t)(rel) : -1;"),
     ("pcp_tail_before_head", C,
      "const int64_t chunks[2] = {k, 2 * K - 1 - k};", "const int64_t chunks[2] = {2 * K - 1 - k, k};"),
     # storage decoding
@@ -143,6 +145,8 @@ MUTANTS = [
      "            i = t * B + b\n            C = cand[i][cand[i] >= 0]"),
     ("sparse_localize_keeps_global_position", PY,
      "local[r, i, counts[r, i]] = lp[t]", "local[r, i, counts[r, i]] = t"),
+    ("sparse_count_not_advanced", PY,
+     "            counts[r, i] += 1", "            counts[r, i] = 1"),
     ("sparse_rank_filter_inverted", PY,
      "C = C[layouts[L][0][C] == rank]", "C = C[layouts[L][0][C] != rank]"),
     ("sparse_query_of_the_first_token", PY,
