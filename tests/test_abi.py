@@ -325,3 +325,34 @@ def test_binding_size_checks_cover_the_other_entry_points(libdcp):
         dcp.dcp_sparse_decode_attention(m, q, torch.zeros((B, k), **i32), torch.zeros((10, 64, 575), dtype=torch.uint8),
                                         10, torch.zeros((8, B, M), **i32), seq,
                                         torch.zeros((B, 1, 128, 512), dtype=torch.bfloat16))
+
+
+def test_a_plain_c_program_compiles_links_and_calls_the_library(libdcp, tmp_path):
+    """The boundary is a C ABI: a C99 program that includes include/dcp.h,
+    links libdcp.so and calls the entry points that need no device (version,
+    error strings, host validation) works without any C++ or torch."""
+    import shutil
+    import subprocess
+    from context_decode_attention_gb300 import build
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "caller.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "dcp.h"\n'
+        "int main(void) {\n"
+        "    dcp_params p = {0};  /* N = 0: rejected by host validation, no device touched */\n"
+        "    size_t n = 0;\n"
+        "    int rc = dcp_workspace_size(&p, 1, 1, &n);\n"
+        '    printf("%d %d %s\\n", dcp_version(), rc, dcp_error_string(rc));\n'
+        "    return 0;\n"
+        "}\n")
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(build.LIB)
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src),
+                        "-L", libdir, "-ldcp", f"-Wl,-rpath,{libdir}", "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "1 1 invalid argument"
