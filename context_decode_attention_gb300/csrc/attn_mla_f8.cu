@@ -22,8 +22,12 @@
 //     and the residual the other 4), and the rest to within 2^-10 of a row
 //     maximum of at least 224;
 //   * the probabilities p' = 2^(s - m_ref + kPBias) <= 2^8: hi + lo keeps
-//     about 8 significant bits (the residual goes through fp16), and values
-//     below 2^-10, more than 15 binades under the running maximum, vanish.
+//     about 8 significant bits (the residual goes through fp16) down to
+//     2^-6; below that the absolute error is at most 2^-10 (values under
+//     2^-10 vanish).  The reference follows the tiles both ways (a tile's
+//     maximum stays above 2^(kPBias - kLowerLog2)), so a token is lost only
+//     when it lies more than 15 - kLowerLog2 binades below the maximum of its
+//     own 128-token tile, and a tile loses at most 127 such tokens.
 // All products accumulate in fp32 in tensor memory.
 //
 // Work split as in the bf16 kernel: two CTAs share a token range, each owning
@@ -84,8 +88,16 @@ constexpr int kOffTiles = kOffUnits + kUnits * 8;
 constexpr int kSmem = kOffTiles + kTileRing * 16;  // the dynamic buffer is 1024-byte aligned (checked at entry)
 static_assert(kUnits <= kUnitCache, "unit cache");
 static_assert(kSmem <= 232448, "shared memory");
-// lazy softmax reference (log2 units) and the bias that keeps p' in e4m3 range
+// Softmax reference (log2 units), kept lazily in both directions: it moves up
+// when a tile's maximum passes it by more than kRescaleLog2 (p' would leave
+// e4m3's range) and down to the tile's maximum when that lies more than
+// kLowerLog2 below it (a tile far below the reference would otherwise fall
+// under e4m3's smallest step and vanish from P.V), as long as the largest
+// weight seen stays within 2^kMaxSpanLog2 of the new reference (fp32 O and l
+// then cannot overflow).  kPBias keeps p' = 2^(s - m_ref + kPBias) <= 2^8.
 constexpr float kRescaleLog2 = 3.f;
+constexpr float kLowerLog2 = 4.f;
+constexpr float kMaxSpanLog2 = 64.f;
 constexpr float kPBias = 5.f;
 
 // One tile as the producers saw it, for the MMA issuer (which then needs no
@@ -482,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool alive = true;
         Tile prev{}, t{};
         int ti = 0;
-        float m_ref = -INFINITY, l = 0.f;
+        float m_ref = -INFINITY, m_top = -INFINITY, l = 0.f;
         const float sl2 = a.softmax_scale * a.kv_scale * 1.4426950408889634f;
         float sl2h = sl2;  // sl2 times this head's query scale
         float* part_o = reinterpret_cast<float*>(a.ws + a.lay.off_part_o);
@@ -535,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int b = (int)((uint32_t)t.u / (uint32_t)a.N);
                 sl2h = sl2 * qscale[((int64_t)b * a.Tq + tq) * kHeads + h];
-                m_ref = -INFINITY;
+                m_ref = m_top = -INFINITY;
                 l = 0.f;
             }
             const int sb = ti & 1;
@@ -572,11 +584,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             float corr = 1.f;
             bool rescale_o = false;
             if (mx > -INFINITY) {
+                m_top = fmaxf(m_top, mx);
                 if (m_ref == -INFINITY) {
                     m_ref = mx;  // first visible tokens of the segment: O not yet accumulated
                     corr = 0.f;
-                } else if (mx > m_ref + kRescaleLog2) {
-                    corr = ex2_approx(m_ref - mx);
+                } else if (mx > m_ref + kRescaleLog2 || (mx < m_ref - kLowerLog2 && m_top - mx <= kMaxSpanLog2)) {
+                    corr = ex2_approx(m_ref - mx);  // < 1 up, > 1 down
                     m_ref = mx;
                     rescale_o = true;
                 }

@@ -115,7 +115,6 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0,
                  : "memory");
 }
 
-// 2^x on the SFU (ex2.approx.ftz: ~2 ulp; -inf -> +0).
 // two fp32 lanes in one 64-bit register pair, and the paired FMA / add of
 // sm_100-class SMs (one instruction for two columns of a softmax pass)
 __device__ __forceinline__ uint64_t pair_f32(float lo, float hi) {
@@ -143,6 +142,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
+// 2^x on the SFU (ex2.approx.ftz: ~2 ulp; -inf -> +0).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -228,3 +228,48 @@ def sparse_candidates(wl: Workload, k: int, seed: int = 0) -> np.ndarray:
             pick = np.arange(vis) if vis <= k else np.sort(rng.choice(vis, size=k, replace=False))
             out[b * Tq + t, :len(pick)] = pick
     return out
+
+
+def sink_tail_workload(cfg: dict, sink_positions, gaps_nats, seed: int = 0) -> Workload:
+    """A peaked long-context input for the MLA layout (one request, Tq = 1):
+    one strongly attended key (an "attention sink") at each of
+    sink_positions, and a long flat tail of identical keys whose values have
+    a nonzero mean, so that the tail's many small weights carry a share of
+    the softmax mass that an output must not lose.
+
+    Recipe (values before rounding to the storage dtype):
+      * tail row: value columns c < Dv hold 0.5 + 0.25 cos(c), RoPE columns 0;
+      * sink row: value columns -1 + 0.25 sin(c), RoPE columns 1.5;
+      * query head h: latent columns 0, RoPE columns g_h with
+        g_h = gaps_nats[h] / (softmax_scale * 1.5 * (Dk - Dv)), so that head h
+        scores a sink about gaps_nats[h] nats above every tail token.
+    fp8 uses one per-tensor scale amax / 448 = 1.5 / 448 (the sink's RoPE
+    columns store 448 exactly).  `seed` only labels the workload (block
+    permutation); nothing here is random.
+    """
+    B, Tq, Hq, Hkv = (int(cfg[k]) for k in ("B", "Tq", "Hq", "Hkv"))
+    Dk, Dv = int(cfg["Dk"]), int(cfg["Dv"])
+    assert cfg["layout"] == "mla" and B == 1 and Tq == 1 and Hkv == 1
+    seq_lens = draw_lengths(cfg, None)
+    L = int(seq_lens[0])
+    gaps = np.asarray(gaps_nats, dtype=np.float64)
+    assert gaps.shape == (Hq,)
+    c = np.arange(Dk)
+    tail = np.where(c < Dv, 0.5 + 0.25 * np.cos(c), 0.0).astype(np.float32)
+    sink = np.where(c < Dv, -1.0 + 0.25 * np.sin(c), 1.5).astype(np.float32)
+    kv_dtype = cfg["kv_dtype"]
+    scale = float(np.float32(1.5) / np.float32(448.0)) if kv_dtype == "fp8" else 1.0
+    tail_raw = _round(tail[None, None, :], kv_dtype, scale)[0, 0]
+    sink_raw = _round(sink[None, None, :], kv_dtype, scale)[0, 0]
+    k = np.empty((L, 1, Dk), dtype=_np_dtype(kv_dtype))
+    k[:, 0, :] = tail_raw
+    for p in sink_positions:
+        assert 0 <= int(p) < L
+        k[int(p), 0, :] = sink_raw
+    g = gaps / (float(cfg["softmax_scale"]) * 1.5 * (Dk - Dv))
+    qf = np.zeros((B, Tq, Hq, Dk), dtype=np.float32)
+    qf[0, 0, :, Dv:] = g[:, None].astype(np.float32)
+    q = _round(qf, cfg["q_dtype"])
+    req_start = np.array([0, L], dtype=np.int64)
+    return Workload(cfg=dict(cfg), seed=int(seed), seq_lens=seq_lens, req_start=req_start, q=q, k=k, v=None,
+                    kv_scale=scale, extra={"sink_positions": [int(p) for p in sink_positions]})

@@ -88,3 +88,84 @@ def test_probability_split_bound():
     # about bf16's precision where the residual stays normal
     big = p >= 2.0 ** -2
     assert torch.all(err[big] <= (2.0 ** -8 + 2.0 ** -11) * p[big])
+
+
+# ---------------------------------------------------------------------------
+# The softmax reference across tiles.  A model of the fp8 kernel's per-tile
+# step (its constants: tiles of 128 tokens, p' = 2^(s - m_ref + 5), the
+# reference raised when a tile's maximum passes it by more than 3 binades and
+# lowered to the tile's maximum when that lies more than 4 binades below it),
+# with hi + lo formed as above; l sums the fp32 p'.  Scores are in log2 units.
+
+TILE, UP, DOWN, BIAS = 128, 3.0, 4.0, 5.0
+
+
+def _split_sum(p):
+    ph = torch.from_numpy(p.astype(np.float32)).to(torch.float16).to(torch.float64)
+    hi = _e4m3(ph)
+    return (hi + _e4m3(ph - hi)).numpy()
+
+
+def _tiled_softmax_weights(s2, lower):
+    """Represented weights (what P.V sees) and fp32 row sum, both relative to
+    the final reference, for scores s2 walked tile by tile."""
+    m_ref, m_top = -np.inf, -np.inf
+    rep, lsum = [], 0.0
+    for t0 in range(0, len(s2), TILE):
+        s = s2[t0:t0 + TILE]
+        mx = s.max()
+        m_top = max(m_top, mx)
+        corr = 1.0
+        if m_ref == -np.inf:
+            m_ref, corr = mx, 0.0
+        elif mx > m_ref + UP or (mx < m_ref - lower and m_top - mx <= 64.0):
+            corr, m_ref = 2.0 ** (m_ref - mx), mx
+        rep = [r * corr for r in rep]
+        lsum = lsum * corr
+        p = (2.0 ** (s - m_ref + BIAS)).astype(np.float32).astype(np.float64)
+        rep.append(_split_sum(p))
+        lsum += p.sum()
+    return np.concatenate(rep), lsum
+
+
+def test_one_way_reference_loses_a_flat_tail_two_way_keeps_it():
+    # a sink 12 nats above 32K identical tail tokens: the tail carries ~17 % of
+    # the mass, each tail token 2^-17.3 of the sink.  One-way, every tail tile
+    # stays at the sink's reference and vanishes; two-way, only the 127 tail
+    # tokens that share the sink's tile do (plus the split's rounding)
+    n = 32768
+    s2 = np.zeros(n)
+    s2[0] = 12.0 * np.log2(np.e)
+    for lower, lost_at_least, lost_at_most in [(np.inf, 0.15, 1.0), (DOWN, 0.0, 127 / (n - 1) + 2.0 ** -8)]:
+        rep, lsum = _tiled_softmax_weights(s2, lower)
+        tail_share_true = (n - 1) * np.exp(-12.0) / (1 + (n - 1) * np.exp(-12.0))
+        tail_share_rep = rep[1:].sum() / lsum
+        lost = (tail_share_true - tail_share_rep) / tail_share_true
+        assert lost_at_least <= lost <= lost_at_most, (lower, lost)
+
+
+def test_two_way_reference_aggregate_bound():
+    """Against the row sum, the weight that P.V misses (or gets wrong) stays
+    below the per-tile bound: a token is off by at most 2^-10 (p' units) below
+    p' = 2^-6 and by (2^-8 + 2^-11) p' above, and a tile whose maximum sits at
+    p' >= 2^(5 - DOWN) holds 127 other tokens at most, so the missing share is
+    below 127 * 2^-10 / 2^(5 - DOWN) + 2^-8 + 2^-11 of the row sum."""
+    rng = np.random.default_rng(11)
+    bound = 127 * 2.0 ** -10 / 2.0 ** (BIAS - DOWN) + 2.0 ** -8 + 2.0 ** -11
+    worst = 0.0
+    for trial in range(60):
+        ntiles = int(rng.integers(2, 40))
+        s2 = []
+        for _ in range(ntiles):
+            # adversarial tiles: one maximum, the rest just under the vanishing
+            # point relative to a maximum that sits anywhere within the window
+            top = rng.uniform(-DOWN, UP) + (0.0 if trial % 3 else rng.uniform(-30, 30))
+            depth = rng.uniform(10.0, 16.0, TILE - 1)
+            s2.append(np.concatenate([[top], top - depth]))
+        s2 = np.concatenate(s2)
+        rep, lsum = _tiled_softmax_weights(s2, DOWN)
+        # both sides relative to the final reference: the fp32 row sum is exact enough here
+        miss = abs(lsum - rep.sum()) / lsum
+        worst = max(worst, miss)
+        assert miss <= bound, (trial, miss, bound)
+    assert worst > 0.0

@@ -293,3 +293,36 @@ def test_transfer_blocks_many_requests_and_repeated_calls(N, I, bs, B):
             assert np.array_equal(g, ref[key]), (rep, key)
     assert dcp.dcp_get_error(ws) == 0
     assert not ws.cpu().numpy().any()  # the header's accumulators are back to zero
+
+
+# ------------------------------------------------- peaked long contexts
+
+@pytest.mark.parametrize("kv_dtype", ["fp8", "bf16"])
+def test_long_flat_tail_below_a_sink(kv_dtype):
+    """One 256K-token request on 8 ranks (32K tokens per rank) whose keys are
+    a flat tail of identical rows (values with mean ~0.5) except two sinks
+    (token 3 and token 100,000: ranks 3 and 0), which the 128 query heads
+    score 6 to 20 nats above the tail.  Each tail token then weighs e^-6 to
+    e^-20 of a sink, yet together the tail carries up to half of its rank's
+    softmax mass, so an output that loses small probabilities (a two-term
+    e4m3 split that underflows) misses that share.  Merged output and the
+    sink ranks' partials, every element, against the oracle; the bf16 cache
+    runs the same case as a control."""
+    from context_decode_attention_gb300.harness import DeviceWorkload
+    from dcp_workloads import sink_tail_workload
+    cfg = config("mla_fp8_mixed" if kv_dtype == "fp8" else "mla_bf16_32k", B=1, I=1,
+                 lengths=("list", [262144]))
+    wl = sink_tail_workload(cfg, [3, 100000], np.linspace(6.0, 20.0, int(cfg["Hq"])), seed=4)
+    dw = DeviceWorkload(wl)
+    out, lse = dw.decode()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    ref_o, ref_l = oracle.attention(wl)
+    assert_close_rows(f64(out).reshape(ref_o.shape), f64(lse).reshape(-1), ref_o, ref_l, tol_for(cfg),
+                      f"{kv_dtype} sink + flat tail")
+    op, lp = dw.partial()
+    torch.cuda.synchronize()
+    for r in (3, 0):
+        ref_o, ref_l = oracle.attention(wl, rank=r)
+        assert_close_rows(f64(op[r]).reshape(ref_o.shape), f64(lp[r]).reshape(-1), ref_o, ref_l, tol_for(cfg),
+                          f"{kv_dtype} sink + flat tail, rank {r}")
