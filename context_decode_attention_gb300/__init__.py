@@ -8,7 +8,8 @@ back to the CPU: if the library is missing or cannot load, every call raises.
 Functions carry the C ABI's names (include/dcp.h):
   dcp_workspace_size, dcp_workspace_init, dcp_get_error, dcp_slot_mapping, dcp_transfer_blocks, dcp_pcp_partition, dcp_prefill_attention,
   dcp_sparse_workspace_size, dcp_sparse_localize, dcp_sparse_decode_attention,
-  dcp_partial_attention, dcp_lse_merge, dcp_decode_attention, dcp_decode_attention_noalloc
+  dcp_partial_attention, dcp_lse_merge, dcp_decode_attention, dcp_decode_attention_noalloc,
+  dcp_noalloc_get_error
 """
 
 import ctypes
@@ -24,7 +25,7 @@ __all__ = [
     "dcp_workspace_size", "dcp_workspace_init", "dcp_get_error", "dcp_slot_mapping", "dcp_transfer_blocks", "dcp_pcp_partition",
     "dcp_prefill_attention", "dcp_sparse_workspace_size", "dcp_sparse_localize", "dcp_sparse_decode_attention",
     "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention", "dcp_decode_attention_noalloc",
-    "dcp_launch_count",
+    "dcp_noalloc_get_error", "dcp_launch_count",
     "dcp_attention_kernel", "DCP_F32", "DCP_BF16", "DCP_FP8_E4M3", "DCP_LAYOUT_GQA", "DCP_LAYOUT_MLA",
 ]
 
@@ -325,3 +326,12 @@ def dcp_decode_attention_noalloc(params, q, k_pool, v_pool, num_blocks, block_ta
                                               int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(local_lens),
                                               _ptr(out), _ptr(lse), _stream(stream)),
            "dcp_decode_attention_noalloc")
+
+
+def dcp_noalloc_get_error(stream=None):
+    """Device error bits the last dcp_decode_attention_noalloc call on this
+    device left in the library's static buffer (read and cleared; waits for
+    the stream).  Allocates nothing."""
+    bits = ctypes.c_uint32(0)
+    _check(lib().dcp_noalloc_get_error(_stream(stream), ctypes.byref(bits)), "dcp_noalloc_get_error")
+    return int(bits.value)

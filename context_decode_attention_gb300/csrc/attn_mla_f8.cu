@@ -80,7 +80,7 @@ constexpr int kOffQTail = 8 * kSubBytes;
 constexpr int kQBytes = 9 * kSubBytes;  // 147456
 constexpr int kOffRing = kQBytes;
 constexpr int kOffBar = kOffRing + kRing * kSubBytes;
-constexpr int kNumBars = 2 * kRing + 7;
+constexpr int kNumBars = 2 * kRing + 8;
 constexpr int kOffUnits = kOffBar + kNumBars * 8 + 16;
 constexpr int kUnits = 64;      // cached unit-prefix entries (kUnitCache at most)
 constexpr int kTileRing = 8;    // tile descriptors handed from the producers to the MMA issuer
@@ -108,7 +108,7 @@ struct TileMsg {
 };
 
 struct Bars {
-    uint64_t *full, *empty, *q_full, *q_empty, *s_full, *p_full, *o_done;
+    uint64_t *full, *empty, *q_full, *q_empty, *s_full, *p_full, *o_done, *drain;
     uint32_t* tmem_slot;
 };
 
@@ -122,6 +122,7 @@ __device__ __forceinline__ Bars carve(uint8_t* base) {
     s.s_full = b; b += 2;
     s.p_full = b; b += 2;
     s.o_done = b++;
+    s.drain = b++;
     s.tmem_slot = reinterpret_cast<uint32_t*>(b);
     return s;
 }
@@ -284,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.p_full[i], kSoftmaxWarps);
         }
         mbar_init(sh.o_done, 1);
+        mbar_init(sh.drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_kv);
@@ -397,6 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (bad_block) raise_err(err, DCP_DEV_ERR_BLOCK_ID);
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+            // on a timeout, give this warp's TMA copies time to land before the
+            // CTA exits (a copy completes within microseconds)
+            if (!alive) tma_drain_pause();
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
@@ -484,6 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ti;
             }
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+            // every MMA this thread issued has completed before the CTA releases
+            // tensor memory (also when a role stopped early on a timeout)
+            mma_commit(sh.drain);
+            mbar_wait_sleep(sh.drain, 0);
         }
     } else {
         // ------------------------------------------------------------ softmax warpgroup

@@ -60,7 +60,7 @@ constexpr int kRing = 5;
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kQBytes;
 constexpr int kOffBar = kOffRing + kRing * kSubBytes;
-constexpr int kNumBars = 2 * kRing + 7;
+constexpr int kNumBars = 2 * kRing + 8;
 constexpr int kOffUnits = kOffBar + kNumBars * 8 + 16;
 constexpr int kTileRing = 8;  // tile descriptors handed from the producers to the MMA issuer
 constexpr int kOffTiles = kOffUnits + kUnitCache * 8;
@@ -75,7 +75,7 @@ struct TileMsg {
 };
 
 struct Bars {
-    uint64_t *full, *empty, *q_full, *q_empty, *s_full, *p_full, *o_done;
+    uint64_t *full, *empty, *q_full, *q_empty, *s_full, *p_full, *o_done, *drain;
     uint32_t* tmem_slot;
 };
 
@@ -89,6 +89,7 @@ __device__ __forceinline__ Bars carve(uint8_t* base) {
     s.s_full = b; b += 2;
     s.p_full = b; b += 2;
     s.o_done = b++;
+    s.drain = b++;
     s.tmem_slot = reinterpret_cast<uint32_t*>(b);
     return s;
 }
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.p_full[i], 4);
         }
         mbar_init(sh.o_done, 1);
+        mbar_init(sh.drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_kv);
@@ -253,6 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (bad_block) raise_err(err, DCP_DEV_ERR_BLOCK_ID);
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+            // on a timeout, give this warp's TMA copies time to land before the
+            // CTA exits (a copy completes within microseconds)
+            if (!alive) tma_drain_pause();
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
@@ -330,6 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ti;
             }
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+            // every MMA this thread issued has completed before the CTA releases
+            // tensor memory (also when a role stopped early on a timeout)
+            mma_commit(sh.drain);
+            mbar_wait_sleep(sh.drain, 0);
         }
     } else {
         // ------------------------------------------------------------ softmax warpgroup

@@ -62,7 +62,7 @@ constexpr int kMaxPages = 32;                // pages a tile may touch: kKeys / 
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kQBytes;
 constexpr int kOffBar = kOffRing + kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 1 + 2 + 2 + 1;
+constexpr int kNumBars = 2 * kStages + 1 + 2 + 2 + 1 + 1;
 constexpr int kOffKv = kOffBar + kNumBars * 8 + 16;     // after the barriers and the TMEM address
 constexpr int kOffBlk = kOffKv + 16;                    // [kProd][32] block ids of the producers' current tile
 constexpr int kOffXch = kOffBlk + kProd * 32 * 4;       // [2][kSoftGroups][kRows] floats
@@ -70,7 +70,7 @@ constexpr int kSmem = kOffXch + 2 * kSoftGroups * kRows * 4;
 static_assert(kSmem <= 232448, "shared memory");
 
 struct Bars {
-    uint64_t *full, *empty, *q_full, *s_full, *p_full, *o_done;
+    uint64_t *full, *empty, *q_full, *s_full, *p_full, *o_done, *drain;
     uint32_t* tmem_slot;
 };
 
@@ -83,6 +83,7 @@ __device__ __forceinline__ Bars carve(uint8_t* base) {
     s.s_full = b; b += 2;
     s.p_full = b; b += 2;
     s.o_done = b++;
+    s.drain = b++;
     s.tmem_slot = reinterpret_cast<uint32_t*>(b);
     return s;
 }
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.p_full[i], 4 * kSoftGroups);
         }
         mbar_init(sh.o_done, 1);
+        mbar_init(sh.drain, 1);
         fence_mbar_init();
         s_kv = 0;
     }
@@ -251,6 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (bad) raise_err(err, DCP_DEV_ERR_BLOCK_ID);
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+            // on a timeout, give this warp's TMA copies time to land before the
+            // CTA exits (a copy completes within microseconds)
+            if (!alive) tma_drain_pause();
         }
     } else if (warp < kProd) {
         // ------------------------------------------------------------ cp.async producers
@@ -361,6 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (alive && !pv(ntiles - 1)) alive = false;
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+            // every MMA this thread issued has completed before the CTA releases
+            // tensor memory (also when a role stopped early on a timeout)
+            mma_commit(sh.drain);
+            mbar_wait_sleep(sh.drain, 0);
         }
     } else {
         // ------------------------------------------------------------ softmax warpgroups

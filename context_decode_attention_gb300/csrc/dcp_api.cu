@@ -290,6 +290,7 @@ int dcp_slot_mapping(const dcp_params* params, int32_t B, const int32_t* seq_len
     if (B < 0 || T < 0) return DCP_ERR_INVALID_ARG;
     if (B > 0 && !seq_lens) return DCP_ERR_INVALID_ARG;
     if (T > 0 && (owner || slots || new_k) && (!tok_req || !tok_pos)) return DCP_ERR_INVALID_ARG;
+    if (owner && p.N > 127) return DCP_ERR_INVALID_ARG;  // owner ranks are stored as int8
     if (T > 0 && B == 0 && (owner || slots || new_k)) return DCP_ERR_INVALID_ARG;
     if ((slots || new_k) && (!block_tables || max_blocks < 1 || num_blocks < 1)) return DCP_ERR_INVALID_ARG;
     if (new_k && !k_pool) return DCP_ERR_INVALID_ARG;
@@ -510,6 +511,14 @@ void* static_scratch() {
 
 }  // namespace
 }  // namespace dcp
+
+extern "C" int dcp_noalloc_get_error(cudaStream_t stream, uint32_t* bits) {
+    if (!bits) return DCP_ERR_INVALID_ARG;
+    void* ws = static_scratch();
+    if (ws == nullptr) return DCP_ERR_CUDA;
+    // the same read-and-clear as dcp_get_error, on the library's own buffer
+    return dcp_get_error(ws, stream, bits);
+}
 
 extern "C" int dcp_decode_attention_noalloc(const dcp_params* params, int32_t B, const void* q,
                                             const void* k_pool, const void* v_pool, int64_t num_blocks,

@@ -86,6 +86,12 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity) 
     return mbar_try_wait_sleep(bar, parity) || mbar_wait_sleep_slow(bar, parity);
 }
 
+// A bounded pause (~64 us) for a producer that stopped early: its TMA copies
+// in flight land in shared memory before the CTA exits.
+__device__ __forceinline__ void tma_drain_pause() {
+    for (int i = 0; i < 64; ++i) __nanosleep(1000);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

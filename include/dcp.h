@@ -162,7 +162,8 @@ int dcp_get_error(void* workspace, cudaStream_t stream, uint32_t* bits);
  * index >= max_blocks -> DCP_DEV_ERR_TABLE; block id outside
  * [0, num_blocks) -> DCP_DEV_ERR_BLOCK_ID; the token's slots stay -1 and its
  * row is not written.  The workspace needs at least dcp_workspace_size bytes
- * for (params, B).
+ * for (params, B).  owner holds ranks as int8: with owner != NULL, N must be
+ * at most 127 (DCP_ERR_INVALID_ARG otherwise).
  */
 int dcp_slot_mapping(const dcp_params* params, int32_t B, const int32_t* seq_lens,
                      int64_t T, const int32_t* tok_req, const int64_t* tok_pos,
@@ -358,8 +359,9 @@ int dcp_decode_attention(const dcp_params* params, int32_t B, const void* q,
  *  - All calls share the one buffer and it keeps the last call's contents:
  *    calls that overlap on the GPU (other streams, other host threads) race
  *    and corrupt each other's results; serialize them.
- *  - Device-side checks still run, but their error bits stay in the shared
- *    buffer (cleared at the start of each call) and are not reported.
+ *  - Device-side checks still run; their error bits go to the shared
+ *    buffer's error word, which each call clears when it starts.  Read them
+ *    with dcp_noalloc_get_error.
  */
 #define DCP_STATIC_SCRATCH_BYTES (64u << 20)
 int dcp_decode_attention_noalloc(const dcp_params* params, int32_t B, const void* q,
@@ -367,6 +369,15 @@ int dcp_decode_attention_noalloc(const dcp_params* params, int32_t B, const void
                                  const int32_t* block_tables, int32_t max_blocks,
                                  const int32_t* seq_lens, const int32_t* local_lens,
                                  void* out, float* lse, cudaStream_t stream);
+
+/*
+ * The error word of dcp_decode_attention_noalloc's static buffer, for the
+ * same callers (no passage of the pages has a counterpart either): waits for
+ * `stream`, then reads the DCP_DEV_ERR_* bits the most recent call on this
+ * device left (0 = clean) into *bits and clears them, like dcp_get_error does
+ * for a caller's workspace.  Allocates nothing.
+ */
+int dcp_noalloc_get_error(cudaStream_t stream, uint32_t* bits);
 
 #ifdef __cplusplus
 }

@@ -120,6 +120,13 @@ def test_slot_mapping_argument_rules(libdcp):
     rc = libdcp.dcp_slot_mapping(ctypes.byref(p), 2, dummy, 0, None, None, None, 0, 0, None, None, dummy,
                                  None, None, None, None, None, None, dummy, 16, None)
     assert rc == 4
+    # owner ranks are stored as int8: more than 127 ranks with an owner output is refused
+    # (the same call without owner passes these checks; 127 ranks with owner too)
+    for N, owner, want in [(128, dummy, 1), (300, dummy, 1)]:
+        p.N = N
+        rc = libdcp.dcp_slot_mapping(ctypes.byref(p), 2, dummy, 5, dummy, dummy, None, 0, 0, owner, None, None,
+                                     None, None, None, None, None, None, dummy, 1024, None)
+        assert rc == want, (N, rc)
 
 
 @pytest.mark.parametrize("name,kernel", [

@@ -11,6 +11,7 @@ import os
 import socket
 import subprocess
 import sys
+import time
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 ARGS = ["bench.py", "--impl", "reference", "--workload", "gqa_toy", "--steps", "2", "--warmup", "1"]
@@ -27,7 +28,9 @@ def _free_port():
 
 
 def test_reference_arm_prints_the_contract_line():
+    t0 = time.perf_counter()
     r = subprocess.run([sys.executable] + ARGS, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    wall = time.perf_counter() - t0
     assert r.returncode == 0, r.stderr[-2000:]
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
@@ -45,6 +48,11 @@ def test_reference_arm_prints_the_contract_line():
     e2e = ln["e2e"]
     assert e2e["value"] == ln["value"] and e2e["unit"] == ln["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    # the line claims only what ran: its timed steps fit in the process's own
+    # wall time, and the value is marked as scaled up from the samples
+    assert ln["steps"] * ln["ms_per_step"] / 1e3 <= wall
+    ex = ln["extrapolation"]
+    assert ex["timed_region_s"] <= wall and ex["workload_s_extrapolated"] > 0
 
 
 def test_reference_arm_under_torchrun_prints_once():

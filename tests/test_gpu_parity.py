@@ -125,14 +125,27 @@ def test_lse_merge_standalone_random_partials():
     ref_o, ref_l = oracle.merge(o, l)
     od = torch.from_numpy(o.astype(np.float32)).cuda()
     ld = torch.from_numpy(l.astype(np.float32)).cuda()
-    for dt, torch_dt, tol in [(dcp.DCP_F32, torch.float32, (1e-5, 1e-5)), (dcp.DCP_BF16, torch.bfloat16, (2e-2, 1e-5))]:
+    # the oracle merges the same fp32-rounded partials
+    ref_o, ref_l = oracle.merge(o.astype(np.float32).astype(np.float64), l.astype(np.float32).astype(np.float64))
+    for dt, torch_dt in [(dcp.DCP_F32, torch.float32), (dcp.DCP_BF16, torch.bfloat16)]:
         out = torch.empty((rows, Dv), dtype=torch_dt, device="cuda")
         lse = torch.empty(rows, dtype=torch.float32, device="cuda")
         dcp.dcp_lse_merge(N, rows, Dv, od, ld, out, dt, lse)
         torch.cuda.synchronize()
-        # the oracle merges the same fp32-rounded partials
-        ref_o, ref_l = oracle.merge(o.astype(np.float32).astype(np.float64), l.astype(np.float32).astype(np.float64))
-        assert_close_rows(f64(out), f64(lse), ref_o, ref_l, tol, "standalone merge")
+        got_o, got_l = f64(out), f64(lse)
+        assert np.array_equal(np.isneginf(got_l), np.isneginf(ref_l))
+        fin = ~np.isneginf(ref_l)
+        assert np.abs(got_l[fin] - ref_l[fin]).max() <= 1e-5
+        assert np.all(got_o[~fin] == 0.0)
+        # These partials are unnormalised N(0, 1) draws, so the merged outputs
+        # reach |out| ~ 4, where a fixed bf16 bar means little.  The bound is
+        # relative: the fp32 merge is good to ~1e-6 of |out|, and the final
+        # rounding to nearest costs at most half a unit in the last place,
+        # 2^-8 |out| for bf16 (8 significant bits) and 2^-24 |out| for fp32.
+        unit = 2.0 ** -8 if dt == dcp.DCP_BF16 else 2.0 ** -24
+        err = np.abs(got_o[fin] - ref_o[fin])
+        bound = (unit + 2e-6) * np.abs(ref_o[fin]) + 1e-6
+        assert np.all(err <= bound), f"standalone merge: worst err/bound {(err / bound).max():.3g}"
 
 
 @pytest.mark.parametrize("name", ["gqa_bf16_ragged", "mla_fp8_tq4"])
