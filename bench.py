@@ -48,18 +48,18 @@ def load_peaks():
 # the launch's cached tokens; summaries and commands under profiles/).  Valid
 # only for the kernel source they were taken on: a changed source gives null.
 MEASURED_TRAFFIC = {
-    ("mla_tcgen05", "fp8"): ("attn_mla_f8.cu", "68b98a09f8e5560d3bbee06ef8a324c2df3491fe79ef40ecf54a78e24efaeed5",
-                             (218.994944e6 + 4.241664e6) / 376734),
-    ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "f181fb50cf28a8417ae8e36123311d16e8c6be1de275ebd7dc8aacc7be4b9dea",
-                              (304.078336e6 + 4.367360e6) / 262144),
+    ("mla_tcgen05", "fp8"): ("attn_mla_f8.cu", "71bab57997ca90501057b0817eaafd424a78c835d371e0e7beee8becdc05538e",
+                             (219.089920e6 + 4.334336e6) / 376734),
+    ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "59f71d3f4b64aefab5096d5b1bcec05fd692f985ab625a860a98546759ff1abe",
+                              (304.118272e6 + 4.867584e6) / 262144),
     ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "55f1cce0d8111ec459e79dfdc0f0496849629421f35c1b418f54f7e664fe62df",
                           (268.632576e6 + 3.230976e6) / 65536),
     # per table entry (N B max_blocks) of the block-transfer listing
     ("transfer_blocks", "entry"): ("transfer.cu", "ba69fc5af5bf509387a4668d62e0fd322f75cc04daf9e1105750d478aee93893",
                                    (161.792e3 + 0.0) / (8 * 16 * 284)),
     # per request of the prefill workload's shape (2K chunk on a 64K context)
-    ("prefill", "request"): ("attn_prefill_tc.cu", "0ca33f85d5d7aaa267d27097bc8aa7f3af4c0300056cb3163d6de4e6637a2f9f",
-                             294.613248e6 + 112.225280e6),
+    ("prefill", "request"): ("attn_prefill_tc.cu", "8ae5abb4749b2662aa5b93bbdca6bf9d2ec024c60d9065d7701a84ca0bcd33e2",
+                             294.982912e6 + 112.019968e6),
 }
 
 

@@ -339,3 +339,24 @@ def test_long_flat_tail_below_a_sink(kv_dtype):
         ref_o, ref_l = oracle.attention(wl, rank=r)
         assert_close_rows(f64(op[r]).reshape(ref_o.shape), f64(lp[r]).reshape(-1), ref_o, ref_l, tol_for(cfg),
                           f"{kv_dtype} sink + flat tail, rank {r}")
+
+
+@pytest.mark.parametrize("name", ["mla_fp8_tq4", "mla_bf16"])
+def test_mla_output_off_a_16_byte_boundary(name):
+    """An MLA output that starts 2 bytes past a 16-byte boundary: the merge
+    then takes its element-by-element path instead of 16-byte pieces (a
+    different order of the same arithmetic), and must still match the oracle
+    at the stated tolerance."""
+    import context_decode_attention_gb300 as dcp
+    wl, dw = _setup(name)
+    flat = torch.zeros(dw.out.numel() + 1, dtype=dw.out.dtype, device="cuda")
+    out = flat[1:].view(dw.out.shape)
+    assert out.data_ptr() % 16 == 2
+    lse = torch.empty_like(dw.lse)
+    dcp.dcp_decode_attention(dw.params, dw.q, dw.k_pool, dw.v_pool, dw.num_blocks, dw.block_tables, dw.seq_lens,
+                             dw.local_lens, out, lse, dw.workspace)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attention(wl)
+    assert_close_rows(f64(out).reshape(ref_o.shape), f64(lse).reshape(-1), ref_o, ref_l, tol_for(wl.cfg),
+                      f"{name} unaligned output")
+    assert dw.error_bits() == 0
