@@ -48,10 +48,6 @@ def load_peaks():
 # the launch's cached tokens; summaries and commands under profiles/).  Valid
 # only for the kernel source they were taken on: a changed source gives null.
 MEASURED_TRAFFIC = {
-    ("mla_tcgen05", "fp8"): ("attn_mla_f8.cu", "71bab57997ca90501057b0817eaafd424a78c835d371e0e7beee8becdc05538e",
-                             (219.089920e6 + 4.334336e6) / 376734),
-    ("mla_tcgen05", "bf16"): ("attn_mla_tc.cu", "59f71d3f4b64aefab5096d5b1bcec05fd692f985ab625a860a98546759ff1abe",
-                              (304.118272e6 + 4.867584e6) / 262144),
     ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "55f1cce0d8111ec459e79dfdc0f0496849629421f35c1b418f54f7e664fe62df",
                           (268.632576e6 + 3.230976e6) / 65536),
     # per table entry (N B max_blocks) of the block-transfer listing
@@ -644,7 +640,7 @@ def run_sparse(args):
     roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "algorithmic_flops": flops,
                  "algorithmic_bytes": alg_bytes, "roofline_ms": 1e3 * max(t_tc, t_mem),
                  "peak_source": peaks["source"] + " (MEASURED_PEAKS.json, burst)",
-                 "kernel": "sparse localise + stage + mla_f8 (one virtual rank) + merges", "step_ms": ms})
+                 "kernel": "sparse localise + stage + mla_tcgen05 (one virtual rank) + merges", "step_ms": ms})
     line = {
         "metric": SPARSE_METRIC, "value": world * B * Tq / t, "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

@@ -270,16 +270,15 @@ bool gqa_mma_supported(const dcp_params& p);
 int64_t gqa_mma_workers(int num_sms);
 cudaError_t launch_attn_gqa_mma(const AttnArgs& a, cudaStream_t s);
 
-// MLA (128 heads, 576/512 latent, bf16 or fp8 cache) on tcgen05; writes
-// segment partials, then launch_segment_merge combines them.
+// MLA (128 heads, 576/512 latent, bf16 or fp8 cache) on CTA pairs with
+// tcgen05 pair MMAs (attn_mla_pair.cu); writes segment partials, then
+// launch_segment_merge combines them.  The fp8-cache form (kind::f8f6f4,
+// two-term query and probabilities) first runs a query preparation kernel; the
+// prepared query lives in the workspace's qprep region (mla_f8_qprep_bytes).
 bool mla_tc_supported(const dcp_params& p);
 int64_t mla_tc_workers(int num_sms, int Tq);
 cudaError_t launch_attn_mla_tc(const AttnArgs& a, int kv_dtype, cudaStream_t s);
-// the fp8-cache form (kind::f8f6f4, two-term query and probabilities): a query
-// preparation kernel, then the attention kernel; the prepared query lives in
-// the workspace's qprep region (mla_f8_qprep_bytes).
 size_t mla_f8_qprep_bytes(int64_t B, int Tq);
-cudaError_t launch_attn_mla_f8(const AttnArgs& a, cudaStream_t s);
 
 // blocks moved under prefill-decode disaggregation (dcp_transfer_blocks)
 cudaError_t launch_transfer_blocks(int N, int I, int bs, int B, int max_blocks, int64_t num_blocks,

@@ -1,6 +1,6 @@
-// Pieces shared by the two MLA tensor-core kernels (bf16 cache: attn_mla_tc.cu,
-// fp8 cache: attn_mla_f8.cu): the tile walk over a worker's chunk range, the
-// ring-slot counter and the 2D tensor-map encoder.
+// Pieces shared by the MLA tensor-core kernel (attn_mla_pair.cu) and its host
+// check: the tile walk over a worker's chunk range, the ring-slot counter and
+// the 2D tensor-map encoder.
 #pragma once
 
 #include <atomic>
@@ -41,7 +41,7 @@ __device__ __forceinline__ int64_t cache_units(int64_t* us_s, const int64_t* us,
 
 // The same tile sequence in every role (host-callable too, for the CPU check
 // of the walk): walk the worker's chunk range; a tile
-// is up to two consecutive chunks of one unit.  `first` / `last` mark the
+// is up to `maxch` (default two) consecutive chunks of one unit.  `first` / `last` mark the
 // tiles that open and close a merge group inside the range.
 struct TileCursor {
     const int64_t* us;
@@ -49,11 +49,11 @@ struct TileCursor {
     int64_t base, ncache;
     int64_t c, c1, u, ubeg, uend;  // current chunk, range end, unit and its chunk range
     int64_t prev_group;
-    int N, partial;
+    int N, partial, maxch;
     __host__ __device__ void init(const int64_t* us_, const int64_t* us_s_, int64_t ncache_, int64_t c0, int64_t c1_,
-                         int64_t u0, int N_, int pm) {
+                         int64_t u0, int N_, int pm, int maxch_ = 2) {
         us = us_; us_s = us_s_; base = u0; ncache = ncache_;
-        c = c0; c1 = c1_; u = u0; N = N_; partial = pm; prev_group = -1;
+        c = c0; c1 = c1_; u = u0; N = N_; partial = pm; prev_group = -1; maxch = maxch_;
         ubeg = at(u);
         uend = at(u + 1);
     }
@@ -70,7 +70,7 @@ struct TileCursor {
         t.u = u;
         t.chunk = c - ubeg;
         const int64_t end = uend < c1 ? uend : c1;
-        t.n_ch = (end - c) >= 2 ? 2 : 1;
+        t.n_ch = (end - c) >= maxch ? maxch : (int)(end - c);
         t.group = group_of(u);
         c += t.n_ch;
         if (c >= c1) {

@@ -8,7 +8,8 @@
 //     units, per-rank partials or merged groups, a short shared-memory copy of
 //     the unit prefix): every chunk of the range exactly once, in order, each
 //     tile one or two chunks of one unit, and `first` / `last` exactly at the
-//     range's merge-group boundaries.
+//     range's merge-group boundaries (tiles of up to two chunks, and of up
+//     to four for the CTA-pair kernels).
 // Prints "ok" and exits 0, or names the first violated property and exits 1.
 #include <cstdio>
 #include <random>
@@ -42,7 +43,8 @@ int main() {
         }
     }
     // tile walk
-    for (int it = 0; it < 20000; ++it) {
+    for (int it = 0; it < 40000; ++it) {
+        const int maxch = (it & 1) ? 4 : 2;
         const int N = 1 + (int)(rng() % 8), B = 1 + (int)(rng() % 6), pm = (int)(rng() % 2);
         const int U = N * B;
         std::vector<int64_t> us(U + 1, 0);
@@ -58,17 +60,17 @@ int main() {
             const int ncache = (int)(rng() % 5);
             for (int i = 0; i < ncache && u0 + i <= U; ++i) cache.push_back(us[u0 + i]);
             TileCursor cur;
-            cur.init(us.data(), cache.data(), (int64_t)cache.size(), c0, c1, u0, N, pm);
+            cur.init(us.data(), cache.data(), (int64_t)cache.size(), c0, c1, u0, N, pm, maxch);
             Tile t;
             int64_t c = c0, prev_group = -1;
             bool prev_last = true;
             while (cur.next(t)) {
-                if (t.n_ch < 1 || t.n_ch > 2) return fail("tile size", it);
+                if (t.n_ch < 1 || t.n_ch > maxch) return fail("tile size", it);
                 if (!(us[t.u] <= c && c + t.n_ch <= us[t.u + 1]) || us[t.u] + t.chunk != c)
                     return fail("tile chunks", it);
                 if (t.group != (pm ? t.u : t.u / N)) return fail("group", it);
-                // a one-chunk tile only where the range or the unit ends
-                if (t.n_ch == 1 && c + 1 < c1 && c + 1 < us[t.u + 1]) return fail("missed pair", it);
+                // a short tile only where the range or the unit ends
+                if (t.n_ch < maxch && c + t.n_ch < c1 && c + t.n_ch < us[t.u + 1]) return fail("short tile", it);
                 if (t.first != (t.group != prev_group)) return fail("first", it);
                 if (t.first && !prev_last) return fail("group reopened", it);
                 c += t.n_ch;

@@ -92,12 +92,12 @@ def test_probability_split_bound():
 
 # ---------------------------------------------------------------------------
 # The softmax reference across tiles.  A model of the fp8 kernel's per-tile
-# step (its constants: tiles of 128 tokens, p' = 2^(s - m_ref + 5), the
+# step (its constants: tiles of 256 tokens, p' = 2^(s - m_ref + 5), the
 # reference raised when a tile's maximum passes it by more than 3 binades and
 # lowered to the tile's maximum when that lies more than 4 binades below it),
 # with hi + lo formed as above; l sums the fp32 p'.  Scores are in log2 units.
 
-TILE, UP, DOWN, BIAS = 128, 3.0, 4.0, 5.0
+TILE, UP, DOWN, BIAS = 256, 3.0, 4.0, 5.0
 
 
 def _split_sum(p):
@@ -131,12 +131,12 @@ def _tiled_softmax_weights(s2, lower):
 def test_one_way_reference_loses_a_flat_tail_two_way_keeps_it():
     # a sink 12 nats above 32K identical tail tokens: the tail carries ~17 % of
     # the mass, each tail token 2^-17.3 of the sink.  One-way, every tail tile
-    # stays at the sink's reference and vanishes; two-way, only the 127 tail
-    # tokens that share the sink's tile do (plus the split's rounding)
+    # stays at the sink's reference and vanishes; two-way, only the TILE - 1
+    # tail tokens that share the sink's tile do (plus the split's rounding)
     n = 32768
     s2 = np.zeros(n)
     s2[0] = 12.0 * np.log2(np.e)
-    for lower, lost_at_least, lost_at_most in [(np.inf, 0.15, 1.0), (DOWN, 0.0, 127 / (n - 1) + 2.0 ** -8)]:
+    for lower, lost_at_least, lost_at_most in [(np.inf, 0.15, 1.0), (DOWN, 0.0, (TILE - 1) / (n - 1) + 2.0 ** -8)]:
         rep, lsum = _tiled_softmax_weights(s2, lower)
         tail_share_true = (n - 1) * np.exp(-12.0) / (1 + (n - 1) * np.exp(-12.0))
         tail_share_rep = rep[1:].sum() / lsum
@@ -148,10 +148,10 @@ def test_two_way_reference_aggregate_bound():
     """Against the row sum, the weight that P.V misses (or gets wrong) stays
     below the per-tile bound: a token is off by at most 2^-10 (p' units) below
     p' = 2^-6 and by (2^-8 + 2^-11) p' above, and a tile whose maximum sits at
-    p' >= 2^(5 - DOWN) holds 127 other tokens at most, so the missing share is
-    below 127 * 2^-10 / 2^(5 - DOWN) + 2^-8 + 2^-11 of the row sum."""
+    p' >= 2^(5 - DOWN) holds TILE - 1 = 255 other tokens at most, so the missing
+    share is below 255 * 2^-10 / 2^(5 - DOWN) + 2^-8 + 2^-11 of the row sum."""
     rng = np.random.default_rng(11)
-    bound = 127 * 2.0 ** -10 / 2.0 ** (BIAS - DOWN) + 2.0 ** -8 + 2.0 ** -11
+    bound = (TILE - 1) * 2.0 ** -10 / 2.0 ** (BIAS - DOWN) + 2.0 ** -8 + 2.0 ** -11
     worst = 0.0
     for trial in range(60):
         ntiles = int(rng.integers(2, 40))
