@@ -41,11 +41,15 @@
 // down to a tile's maximum far below it (so that a long flat tail far under a
 // strong key stays above e4m3's smallest step).
 //
-// Roles (per CTA, 12 warps):
-//   warps 0-2  TMA producers (box b from warp b % 3; warp 0 also the query)
-//   warp 3     TMEM owner; in CTA 0, lane 0 issues every MMA of the pair
-//   warps 4-11 softmax, O^T rescale and segment epilogue (thread = TMEM lane;
-//              two warps per lane quarter, one per half of the heads)
+// Roles (per CTA, 16 warps):
+//   warps 0-2   TMA producers (box b from warp b % 3; warp 0 also the query)
+//   warp 3      TMEM owner; in CTA 0, lane 0 issues every MMA of the pair; in
+//               CTA 1, lane 0 forwards the completion of its P^T to CTA 0
+//   warps 4-7   softmax group A: head maxima, pair exchange and reference
+//               decision of tile i + 1 (one warp per TMEM lane quarter) ...
+//   warps 8-15  ... while group B computes tile i's probabilities, P^T, row
+//               sums, O^T rescale and segment epilogue (thread = TMEM lane;
+//               two warps per lane quarter, one per half of the heads)
 // Shared memory: query half 72 KB | P^T 32 KB | ring of seven 16 KB slots.
 // TMEM (512 columns per CTA): S^T in [0, 256) (bf16: two buffers of 128
 // columns; FP8: one buffer, hi then lo), O^T blocks [256, 384) and [384, 512).
@@ -71,9 +75,12 @@ constexpr int kRing = 7;
 constexpr int kProd = 3;
 constexpr int kWarpMma = kProd;
 constexpr int kWarpSm = kWarpMma + 1;
-constexpr int kSmWarps = 8;             // two per SM sub-partition: lane quarter x head half
+constexpr int kAWarps = 4;              // softmax group A: one warp per lane quarter, all heads
+constexpr int kSmWarps = 8;             // softmax group B: two per SM sub-partition (lane quarter x head half)
+constexpr int kAThreads = 32 * kAWarps;
 constexpr int kSmThreads = 32 * kSmWarps;
-constexpr int kThreads = 32 * kWarpSm + kSmThreads;
+constexpr int kWarpB = kWarpSm + kAWarps;  // group B (probabilities); group A (maxima, references) before it
+constexpr int kThreads = 32 * kWarpB + kSmThreads;
 constexpr int kQBytes = 9 * kBox;      // this CTA's 64 query rows x 1152 bytes
 constexpr int kOffP = kQBytes;
 constexpr int kPBytes = 4 * kBox;      // P^T: 256 tokens x 64 heads (bf16, or e4m3 hi + lo)
@@ -82,7 +89,8 @@ constexpr int kOffRing = kOffP + kPBytes;
 constexpr int kOffMisc = kOffRing + kRing * kSlot;
 constexpr int kUnits = 64;
 constexpr int kTileRing = 8;
-constexpr int kBarSm = 1;              // named barrier of the softmax warps
+constexpr int kBarA = 1;               // named barriers of the two softmax groups
+constexpr int kBarB = 2;
 static_assert(kOffP % 1024 == 0 && kOffRing % 1024 == 0, "swizzled operands need 1024-byte alignment");
 static_assert(kUnits <= kUnitCache, "unit cache");
 
@@ -103,18 +111,28 @@ struct TileMsg {
     int32_t n_ch, first, last, has_next;
 };
 
+// A tile's softmax reference decision, from group A to group B: per head the
+// shift nb (p' = 2^(s sc + nb)), the log2 scale sc, the factor alpha that
+// brings O^T and l to the new reference, and the reference itself.
+struct Decision {
+    alignas(16) float nb[kHeads];
+    alignas(16) float sc[kHeads];
+    alignas(16) float alpha[kHeads];
+    alignas(16) float mref[kHeads];
+    int32_t rescale;  // some head's reference moved
+};
+
 struct Misc {
     uint64_t full[kRing], empty[kRing];
     uint64_t q_full, q_empty, s_full[2], s_free[2], p_full, p_free, p_in, p_peer, xmax[2], xl, drain;
+    uint64_t dec_full[2], dec_free[2];
     uint32_t tmem_slot;
     int32_t abort;
     TileMsg tmsg[kTileRing];
     int64_t units[kUnits];
     alignas(16) float red_max[4][kHeads];
     alignas(16) float red_sum[4][kHeads];
-    alignas(16) float nb[kHeads];
-    alignas(16) float sc[kHeads];
-    alignas(16) float alpha[kHeads];
+    Decision dec[2];
     alignas(16) float linv[kHeads];
     alignas(16) float xbuf[2][kHeads];
     alignas(16) float lbuf[kHeads];
@@ -138,7 +156,7 @@ struct Cfg<true> {                     // e4m3 cache
     static constexpr int kKItems = 5;  // K sub-tiles of 128 columns (the last: 512-575, then zeros)
     static constexpr int kVItems = 4;  // V^T items (block b, token half h): 128 values x 128 tokens
     static constexpr int kCols = 128;
-    static constexpr uint32_t kIdescQK = idesc_e4m3(256, 256, 0, 0);
+    static constexpr uint32_t kIdescQK = idesc_e4m3(256, 128, 0, 0);
     static constexpr uint32_t kIdescPV = idesc_e4m3(256, 128, 1, 1);
 };
 
@@ -146,7 +164,7 @@ struct Cfg<true> {                     // e4m3 cache
 // the warp's 32 lanes of column j: a transposing butterfly in which every
 // exchange halves the columns a lane still carries (31 shuffles in all).
 template <bool kMax>
-__device__ __forceinline__ float xpose_reduce(float (&v)[32]) {
+__device__ __forceinline__ float xpose_reduce(float (&v)[32]) {  // v is consumed
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int w = 16; w >= 1; w >>= 1) {
@@ -157,6 +175,31 @@ __device__ __forceinline__ float xpose_reduce(float (&v)[32]) {
             const float keep = up ? v[k + w] : v[k];
             const float got = __shfl_xor_sync(0xffffffffu, send, w);
             v[k] = kMax ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    return v[0];
+}
+
+// The maximum form of the same butterfly over x[k] (or -inf where !keep),
+// leaving x untouched: its first exchange reads x directly.
+__device__ __forceinline__ float xpose_max(const float (&x)[32], bool keep) {
+    const int lane = threadIdx.x & 31;
+    const bool up = (lane & 16) != 0;
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const float lo = keep ? x[k] : -INFINITY, hi = keep ? x[k + 16] : -INFINITY;
+        const float got = __shfl_xor_sync(0xffffffffu, up ? lo : hi, 16);
+        v[k] = fmaxf(up ? hi : lo, got);
+    }
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1) {
+        const bool u = (lane & w) != 0;
+#pragma unroll
+        for (int k = 0; k < w; ++k) {
+            const float send = u ? v[k] : v[k + w];
+            const float kept = u ? v[k + w] : v[k];
+            v[k] = fmaxf(kept, __shfl_xor_sync(0xffffffffu, send, w));
         }
     }
     return v[0];
@@ -179,8 +222,7 @@ __global__ void __launch_bounds__(256) pair_qprep_kernel(const uint16_t* __restr
 template <bool kF8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_pair_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmap_q,
-                    const __grid_constant__ CUtensorMap tmap_qt, const __grid_constant__ CUtensorMap tmap_kv,
-                    const float* __restrict__ qscale) {
+                    const __grid_constant__ CUtensorMap tmap_kv, const float* __restrict__ qscale) {
     using C = Cfg<kF8>;
     extern __shared__ __align__(1024) uint8_t smem[];
     Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
@@ -217,10 +259,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&ms.q_empty, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms.s_full[i], 1);
-            mbar_init(&ms.s_free[i], 2 * kSmWarps);  // the softmax warps of both CTAs
+            mbar_init(&ms.s_free[i], 2 * kSmWarps);  // group B of both CTAs
             mbar_init(&ms.xmax[i], 1);
+            mbar_init(&ms.dec_full[i], kAWarps);     // group A
+            mbar_init(&ms.dec_free[i], kSmWarps);    // group B
         }
-        mbar_init(&ms.p_full, kSmWarps);  // this CTA's softmax warps
+        mbar_init(&ms.p_full, kSmWarps);  // this CTA's group B
         mbar_init(&ms.p_free, 1);
         mbar_init(&ms.p_in, 1);
         mbar_init(&ms.p_peer, 1);
@@ -229,7 +273,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ms.abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmap_q);
-        if (kF8) tma_prefetch_desc(&tmap_qt);
         tma_prefetch_desc(&tmap_kv);
     }
     if (warp == kWarpMma) {
@@ -319,22 +362,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int b = (int)((uint32_t)cur_t.t.u / (uint32_t)a.N);
                     const int rowq = (int)(((int64_t)b * a.Tq + tq) * kHeads);
                     if (cta == 0) mbar_arrive_expect_tx(&ms.q_full, 2u * kQBytes);
-                    if constexpr (!kF8) {
-                        // heads [64 cta, 64 cta + 64): nine [64 rows x 64 columns] sub-tiles
-                        for (int j = 0; j < 9; ++j)
-                            tma_load_2d_pair(sQ + j * kBox, &tmap_q, C::kCols * j, rowq + 64 * (int)cta, lead_qfull);
-                    } else {
-                        // all 128 heads of this CTA's term (CTA 0 hi, CTA 1 lo; prepared row: hi[0:512]
-                        // lo[0:512] hi[512:576] lo[512:576]): four [128 rows x 128 B] sub-tiles (SW128)
-                        // and the tail [128 rows x 64 B] (SW64)
-                        for (int j = 0; j < 4; ++j)
-                            for (int hr = 0; hr < 2; ++hr)
-                                tma_load_2d_pair(sQ + j * kSlot + hr * kBox, &tmap_q, 512 * (int)cta + 128 * j,
-                                                 rowq + 64 * hr, lead_qfull);
-                        for (int hr = 0; hr < 2; ++hr)
-                            tma_load_2d_pair(sQ + 4 * kSlot + hr * (kBox / 2), &tmap_qt, 1024 + 64 * (int)cta,
-                                             rowq + 64 * hr, lead_qfull);
-                    }
+                    // heads [64 cta, 64 cta + 64): nine [64 rows x 128 B] sub-tiles (bf16:
+                    // 64 columns each; e4m3: the prepared row hi[0:512] lo[0:512] hi[512:576]
+                    // lo[512:576], so sub-tiles 0-3 hi, 4-7 lo, 8 the tail's hi and lo)
+                    for (int j = 0; j < 9; ++j)
+                        tma_load_2d_pair(sQ + j * kBox, &tmap_q, C::kCols * j, rowq + 64 * (int)cta, lead_qfull);
                 }
                 if (cur_t.valid) {
                     if (cta == 0 && (int)(box % kProd) == me) {
@@ -380,11 +412,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ring.n = kRing;
             uint32_t qf_phase = 0, sfree_phase[2] = {0u, 0u}, pfull_phase = 0;
             bool alive = true, more = true;
-            TileMsg prev{}, t{};
-            int ti = 0;
             // descriptors (start address in 16-byte units in the low bits)
             const uint64_t dq = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSW128);
-            const uint64_t dqt = smem_desc(smem_u32(sQ + 4 * kSlot), 16, 512, kLayoutSW64);  // FP8 query tail
             const uint64_t dk = smem_desc(smem_u32(sRing), 16, 1024, kLayoutSW128);
             // V^T items, MN-major: bf16 two 64-value column blocks one box apart
             const uint64_t dv = smem_desc(smem_u32(sRing), kF8 ? 16 : kBox, 1024, kLayoutSW128);
@@ -392,6 +421,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t dp = kF8 ? smem_desc(smem_u32(sP), 16, 512, kLayoutSW64)
                                     : smem_desc(smem_u32(sP), 16, 1024, kLayoutSW128);
             constexpr uint32_t kSlotD = kSlot >> 4, kBoxD = kBox >> 4;
+            TileMsg prev{}, t{};
+            int ti = 0;
             for (;;) {
                 if (more) {
                     if (!mbar_wait_sleep(&ms.full[ring.slot], ring.phase)) { alive = false; break; }
@@ -400,9 +431,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (!mbar_wait_sleep(&ms.q_full, qf_phase)) { alive = false; break; }
                         qf_phase ^= 1u;
                     }
-                    // S^T buffer: bf16 two (tile parity), FP8 one
-                    const int sb = kF8 ? 0 : (ti & 1);
-                    if (ti >= (kF8 ? 1 : 2)) {  // both CTAs' softmax has loaded the buffer's previous tile
+                    const int sb = ti & 1;  // S^T double buffer
+                    if (ti >= 2) {  // both CTAs' group B has read the buffer's previous tile
                         if (!mbar_wait_sleep_cluster(&ms.s_free[sb], sfree_phase[sb])) { alive = false; break; }
                         sfree_phase[sb] ^= 1u;
                     }
@@ -418,13 +448,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             for (int kk = 0; kk < 4; ++kk)
                                 mma_pair_f16(d, ka + 2 * kk, qb + 2 * kk, C::kIdescQK, (s | kk) != 0);
                         } else {
-                            // N = 256: hi (CTA 0's rows) and lo (CTA 1's) of the 128 heads
+                            // query sub-tiles: hi 0-3, lo 4-7; the tail (columns 512-575) holds hi in
+                            // bytes 0-63 and lo in bytes 64-127; each K-step once per term
                             const bool tail = s == C::kKItems - 1;
-                            const uint64_t qb = tail ? dqt : dq + s * kSlotD;
+                            const uint64_t qh = dq + (tail ? 8 * kBoxD : s * kBoxD);
+                            const uint64_t ql = tail ? qh + 4 : dq + (4 + s) * kBoxD;
                             const int nk = tail ? 2 : 4;
 #pragma unroll 1
-                            for (int kk = 0; kk < nk; ++kk)
-                                mma_pair_f8(d, ka + 2 * kk, qb + 2 * kk, C::kIdescQK, (s | kk) != 0);
+                            for (int kk = 0; kk < nk; ++kk) {
+                                mma_pair_f8(d, ka + 2 * kk, qh + 2 * kk, C::kIdescQK, (s | kk) != 0);
+                                mma_pair_f8(d, ka + 2 * kk, ql + 2 * kk, C::kIdescQK, 1u);
+                            }
                         }
                         mma_commit_pair(&ms.empty[ring.slot]);
                         ring.advance();
@@ -434,10 +468,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (t.last) mma_commit_pair(&ms.q_empty);
                 }
                 if (ti > 0) {
-                    // O^T += V^T P^T of the previous tile, once both CTAs wrote its P^T
-                    // P^T of the previous tile complete in both CTAs: this CTA's softmax warps
-                    // (their stores here, their O^T rescale), the part CTA 1 sent here, and
-                    // CTA 1's own (forwarded by its warp 3)
+                    // O^T += V^T P^T of the previous tile, once P^T is complete in both CTAs: this
+                    // CTA's group B (its stores here, its O^T rescale), the part CTA 1 sent here,
+                    // and CTA 1's own (forwarded by its warp 3)
+                    const TileMsg pt = prev;
                     if (!mbar_wait_sleep(&ms.p_full, pfull_phase) || !mbar_wait_sleep_cluster(&ms.p_in, pfull_phase) ||
                         !mbar_wait_sleep_cluster(&ms.p_peer, pfull_phase)) { alive = false; break; }
                     pfull_phase ^= 1u;
@@ -451,8 +485,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             const uint32_t o = tm + 256u + 128u * bb;
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_pair_f16(o, va + kk * (2048 >> 4), dp + (64 * k + 16 * kk) * (128 >> 4),
-                                             C::kIdescPV, !(prev.first && k == 0 && kk == 0));
+                                mma_pair_f16(o, va + kk * (2048 >> 4), dp + (64 * k + 16 * kk) * (128 >> 4), C::kIdescPV,
+                                             !(pt.first && k == 0 && kk == 0));
                         } else {
                             const int bb = it >> 1, hh = it & 1;
                             const uint32_t o = tm + 256u + 128u * bb;
@@ -460,9 +494,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             for (int kk = 0; kk < 4; ++kk) {
                                 const uint32_t tok = 128 * hh + 32 * kk;
                                 mma_pair_f8(o, va + kk * (4096 >> 4), dp + tok * (64 >> 4), C::kIdescPV,
-                                            !(prev.first && hh == 0 && kk == 0));
-                                mma_pair_f8(o, va + kk * (4096 >> 4), dp + (16384 >> 4) + tok * (64 >> 4), C::kIdescPV,
-                                            1u);
+                                            !(pt.first && hh == 0 && kk == 0));
+                                mma_pair_f8(o, va + kk * (4096 >> 4), dp + (16384 >> 4) + tok * (64 >> 4), C::kIdescPV, 1u);
                             }
                         }
                         mma_commit_pair(&ms.empty[ring.slot]);
@@ -497,33 +530,130 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
         }
         if (lane == 0) mbar_wait_sleep(&ms.drain, 0);
+    } else if (warp < kWarpB) {
+        // ------------------------------------------------------------ softmax group A (both CTAs)
+        // Per tile: the head maxima over the pair's visible tokens and the reference
+        // decision, one tile ahead of group B.  Warp qw: TMEM lane quarter qw (tokens
+        // 32 qw ..), all heads; thread 32 qw + lane owns that head's reference.
+        const int qw = warp - kWarpSm;
+        const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
+        const int hown = 32 * qw + lane;
+        const int jrow = 128 * (int)cta + hown;  // this thread's token row of the pair tile
+        uint32_t sf_phase[2] = {0u, 0u}, df_phase[2] = {0u, 0u};
+        Tile t{};
+        int ti = 0;
+        float m_ref = -INFINITY, m_top = -INFINITY, sl2h = 0.f;
+        const float sl2 = a.softmax_scale * (kF8 ? a.kv_scale : 1.f) * 1.4426950408889634f;
+        int64_t bound_u = -1, bound = 0;
+        const uint32_t peer = cta ^ 1u;
+        const uint32_t peer_xbuf = mapa_shared(smem_u32(&ms.xbuf[0][0]), peer);
+        const uint32_t peer_xmax0 = mapa_shared(smem_u32(&ms.xmax[0]), peer);
+        volatile int32_t* abort_flag = &ms.abort;
+        bool alive = true;
+        for (;;) {
+            if (!cur.next(t)) break;
+            if (t.u != bound_u) {
+                // causal bound of this query token in rank r's local positions
+                const int r = (int)((uint32_t)t.u % (uint32_t)a.N), b = (int)((uint32_t)t.u / (uint32_t)a.N);
+                bound = local_len((int64_t)a.seq_lens[b] - a.Tq + tq + 1, r, a.N, a.I);
+                // given local lengths (sparse staging) end the rank's tokens themselves
+                if (a.lens_given) bound = min(bound, (int64_t)a.local_lens[(int64_t)r * a.B + b]);
+                bound_u = t.u;
+            }
+            if (t.first) {
+                m_ref = m_top = -INFINITY;
+                if constexpr (kF8) {
+                    const int b = (int)((uint32_t)t.u / (uint32_t)a.N);
+                    sl2h = sl2 * qscale[((int64_t)b * a.Tq + tq) * kHeads + hown];
+                }
+            }
+            const int sb = ti & 1;
+            bool ok = __all_sync(0xffffffffu, mbar_wait(&ms.s_full[sb], sf_phase[sb]));
+            sf_phase[sb] ^= 1u;
+            tc_fence_after();
+            const bool vis = ok && jrow < kChunk * t.n_ch && t.chunk * kChunk + jrow < bound;
+            const uint32_t sbase = tm + 128u * sb + lane_off;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                if (ok) {
+                    tmem_ld32(sbase + 32u * c, r);
+                    tmem_wait_ld();
+                }
+                ms.red_max[qw][32 * c + lane] = xpose_max(reinterpret_cast<const float(&)[32]>(r), vis);
+            }
+            if (!ok) *abort_flag = 1;
+            named_sync(kBarA, kAThreads);
+            if (*abort_flag) { alive = false; break; }
+            // the decision buffer of this tile's parity: group B is done with tile ti - 2's
+            const int db = ti & 1;
+            if (ti >= 2) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&ms.dec_free[db], df_phase[db]))) *abort_flag = 1;
+                df_phase[db] ^= 1u;
+            }
+            // the pair's maximum of head hown, then its reference
+            const int xp = ti & 1;
+            bool rescale = false;
+            if (hown == 0) mbar_arrive_expect_tx(&ms.xmax[xp], 4u * kHeads);
+            const float cmax = fmaxf(fmaxf(ms.red_max[0][hown], ms.red_max[1][hown]),
+                                     fmaxf(ms.red_max[2][hown], ms.red_max[3][hown]));
+            st_async_b32(peer_xbuf + 4u * (kHeads * xp + hown), __float_as_uint(cmax), peer_xmax0 + 8u * xp);
+            ok = mbar_wait_cluster(&ms.xmax[xp], (uint32_t)((ti >> 1) & 1));
+            const float hs = kF8 ? sl2h : sl2;
+            const float mraw = fmaxf(cmax, ms.xbuf[xp][hown]);
+            const float mx = (mraw > -INFINITY) ? mraw * hs : -INFINITY;
+            float corr = 1.f;
+            if (mx > -INFINITY) {
+                if (m_ref == -INFINITY) {
+                    m_ref = mx;  // first visible tokens of the segment: nothing accumulated yet
+                } else if (kF8 ? (mx > m_ref + kRescaleLog2 ||
+                                  (mx < m_ref - kLowerLog2 && fmaxf(m_top, mx) - mx <= kMaxSpanLog2))
+                               : mx > m_ref + kUpBf16) {
+                    corr = ex2_approx(m_ref - mx);  // < 1 up, > 1 down
+                    m_ref = mx;
+                    rescale = true;
+                }
+                m_top = fmaxf(m_top, mx);
+            }
+            Decision& d = ms.dec[db];
+            d.nb[hown] = (m_ref == -INFINITY) ? 0.f : (kF8 ? kPBias : 0.f) - m_ref;
+            d.sc[hown] = hs;
+            d.alpha[hown] = corr;
+            d.mref[hown] = m_ref;
+            if (!ok) *abort_flag = 1;
+            const bool any_rescale = named_sync_or(kBarA, kAThreads, rescale);
+            if (*abort_flag) { alive = false; break; }
+            if (hown == 0) d.rescale = any_rescale ? 1 : 0;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.dec_full[db]);  // release: this warp's decision entries
+            ++ti;
+        }
+        if (!alive && hown == 0) raise_err(err, DCP_DEV_ERR_TIMEOUT);
     } else {
-        // ------------------------------------------------------------ softmax warps (both CTAs)
-        // Warp (qw, hh): TMEM lane quarter qw (tokens / value rows 32 qw ..), head half hh
-        // (heads 64 hh ..; P^T columns of CTA hh; O^T block hh).  Threads of the warps with
-        // qw < 2 own head 64 hh + 32 qw + lane: its reference and row sum.
-        const int sw = warp - kWarpSm;
+        // ------------------------------------------------------------ softmax group B (both CTAs)
+        // Per tile, with group A's decision: the probabilities, this CTA's P^T columns
+        // (and the peer's, by st.async), the row sums, the O^T rescale and, at a
+        // segment's end, the epilogue.  Warp (qw, hh) as in group A: its P^T columns
+        // live in CTA hh, its O^T rows are block hh's of lane quarter qw.
+        const int sw = warp - kWarpB;
         const int qw = sw & 3, hh = sw >> 2;
         const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
         const int tau = 32 * qw + lane;          // S^T row (token) / O^T row (value) of this thread
         const int jrow = 128 * (int)cta + tau;   // token row of the pair tile (P^T row)
         const bool owner = qw < 2;
-        const int hown = 64 * hh + 32 * qw + lane;  // the head an owner thread keeps
-        const int sm_tid = threadIdx.x - 32 * kWarpSm;
-        uint32_t sf_phase[2] = {0u, 0u}, xl_phase = 0;
+        const int hown = 64 * hh + 32 * qw + lane;  // the head whose row sum an owner keeps
+        const int b_tid = threadIdx.x - 32 * kWarpB;
+        uint32_t sf_phase[2] = {0u, 0u}, dc_phase[2] = {0u, 0u}, xl_phase = 0;
         int pv_done = -1;                        // last tile whose P.V this thread has seen complete
         Tile prev{}, t{};
         int ti = 0;
-        float m_ref = -INFINITY, m_top = -INFINITY, l = 0.f, sl2h = 0.f;
-        const float sl2 = a.softmax_scale * (kF8 ? a.kv_scale : 1.f) * 1.4426950408889634f;
+        float l = 0.f, m_fin = -INFINITY;
         float* part_o = reinterpret_cast<float*>(a.ws + a.lay.off_part_o);
         float* part_lse = reinterpret_cast<float*>(a.ws + a.lay.off_part_lse);
         const int32_t* seg_base = reinterpret_cast<const int32_t*>(a.ws + a.lay.off_seg_base);
         int64_t bound_u = -1, bound = 0;
         const uint32_t peer = cta ^ 1u;
         const uint32_t lead_sfree0 = mapa_shared(smem_u32(&ms.s_free[0]), 0);
-        const uint32_t peer_xbuf = mapa_shared(smem_u32(&ms.xbuf[0][0]), peer);
-        const uint32_t peer_xmax0 = mapa_shared(smem_u32(&ms.xmax[0]), peer);
         const uint32_t peer_lbuf = mapa_shared(smem_u32(&ms.lbuf[0]), peer);
         const uint32_t peer_xl = mapa_shared(smem_u32(&ms.xl), peer);
         const uint32_t peer_pin = mapa_shared(smem_u32(&ms.p_in), peer);
@@ -549,7 +679,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto epilogue = [&](const Tile& g) -> bool {
             bool ok = wait_pv(ti - 1);
             // row sums of both CTAs' tokens
-            if (sm_tid == 0) mbar_arrive_expect_tx(&ms.xl, 4u * kHeads);
+            if (b_tid == 0) mbar_arrive_expect_tx(&ms.xl, 4u * kHeads);
             if (owner) {
                 st_async_b32(peer_lbuf + 4u * hown, __float_as_uint(l), peer_xl);
                 ok = mbar_wait_cluster(&ms.xl, xl_phase) && ok;
@@ -561,13 +691,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float ltot = l + ms.lbuf[hown];
                 ms.linv[hown] = (ltot > 0.f) ? (kF8 ? a.kv_scale : 1.f) / ltot : 0.f;
                 if (cta == 0 && ok) {
-                    const float mu = (m_ref == -INFINITY) ? 0.f : m_ref - (kF8 ? kPBias : 0.f);
+                    const float mu = (m_fin == -INFINITY) ? 0.f : m_fin - (kF8 ? kPBias : 0.f);
                     part_lse[slot * a.rows + tq * kHeads + hown] =
                         (ltot > 0.f) ? (mu + log2f(ltot)) * 0.6931471805599453f : -INFINITY;
                 }
             }
             if (!ok) *abort_flag = 1;
-            named_sync(kBarSm, kSmThreads);
+            named_sync(kBarB, kSmThreads);
             if (*abort_flag) return false;
             // O^T block hh, row tau of this CTA: value 256 hh + 128 cta + tau of every head
             float* dst = part_o + (slot * a.rows + tq * kHeads) * kDv + 256 * hh + 128 * (int)cta + tau;
@@ -586,120 +716,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (;;) {
             if (!cur.next(t)) break;
             if (t.u != bound_u) {
-                // causal bound of this query token in rank r's local positions
                 const int r = (int)((uint32_t)t.u % (uint32_t)a.N), b = (int)((uint32_t)t.u / (uint32_t)a.N);
                 bound = local_len((int64_t)a.seq_lens[b] - a.Tq + tq + 1, r, a.N, a.I);
-                // given local lengths (sparse staging) end the rank's tokens themselves
                 if (a.lens_given) bound = min(bound, (int64_t)a.local_lens[(int64_t)r * a.B + b]);
                 bound_u = t.u;
             }
             if (t.first) {
                 if (ti > 0 && !epilogue(prev)) { alive = false; break; }
-                m_ref = m_top = -INFINITY;
                 l = 0.f;
-                if constexpr (kF8) {
-                    if (owner) {
-                        const int b = (int)((uint32_t)t.u / (uint32_t)a.N);
-                        sl2h = sl2 * qscale[((int64_t)b * a.Tq + tq) * kHeads + hown];
-                        ms.sc[hown] = sl2h;  // published by the barrier after the maxima
-                    }
-                }
             }
-            // this token's scores of heads 64 hh .. 64 hh + 63 into registers; the
-            // chunk-1 loads overlap the chunk-0 reduction; then the TMEM buffer is free
-            const int sb = kF8 ? 0 : (ti & 1);
-            bool ok = __all_sync(0xffffffffu, mbar_wait(&ms.s_full[sb], sf_phase[sb]));
+            // group A's decision for this tile (S^T is then in TMEM: A waited for it)
+            const int sb = ti & 1;
+            bool ok = __all_sync(0xffffffffu, mbar_wait(&ms.dec_full[sb], dc_phase[sb]));
+            dc_phase[sb] ^= 1u;
+            ok = __all_sync(0xffffffffu, mbar_wait(&ms.s_full[sb], sf_phase[sb])) && ok;
             sf_phase[sb] ^= 1u;
             tc_fence_after();
-            const uint32_t sbase = tm + 128u * sb + 64u * hh + lane_off;
+            const Decision& d = ms.dec[sb];
             const bool vis = ok && jrow < kChunk * t.n_ch && t.chunk * kChunk + jrow < bound;
-            float sv[64];
-            {
-                uint32_t r0[32], r1[32];
-                if (ok) {
-                    tmem_ld32(sbase, r0);
-                    if constexpr (kF8) tmem_ld32(sbase + 128u, r1);
-                    tmem_wait_ld();
-                }
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    sv[k] = kF8 ? __uint_as_float(r0[k]) + __uint_as_float(r1[k]) : __uint_as_float(r0[k]);
-                if (ok) {
-                    tmem_ld32(sbase + 32u, r0);
-                    if constexpr (kF8) tmem_ld32(sbase + 160u, r1);
-                }
-                float v[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = vis ? sv[k] : -INFINITY;
-                ms.red_max[qw][64 * hh + lane] = xpose_reduce<true>(v);
-                if (ok) tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    sv[32 + k] = kF8 ? __uint_as_float(r0[k]) + __uint_as_float(r1[k]) : __uint_as_float(r0[k]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster_relaxed(lead_sfree0 + 8u * sb);  // the loads were waited for
-            {
-                float v[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = vis ? sv[32 + k] : -INFINITY;
-                ms.red_max[qw][64 * hh + 32 + lane] = xpose_reduce<true>(v);
-            }
-            if (!ok) *abort_flag = 1;
-            named_sync(kBarSm, kSmThreads);
-            if (*abort_flag) { alive = false; break; }
-            // owners: the pair's maximum of their head, then its reference
-            const int xp = ti & 1;
-            bool rescale = false;
-            if (sm_tid == 0) mbar_arrive_expect_tx(&ms.xmax[xp], 4u * kHeads);
-            if (owner) {
-                const float cmax = fmaxf(fmaxf(ms.red_max[0][hown], ms.red_max[1][hown]),
-                                         fmaxf(ms.red_max[2][hown], ms.red_max[3][hown]));
-                st_async_b32(peer_xbuf + 4u * (kHeads * xp + hown), __float_as_uint(cmax), peer_xmax0 + 8u * xp);
-                ok = mbar_wait_cluster(&ms.xmax[xp], (uint32_t)((ti >> 1) & 1));
-                const float mraw = fmaxf(cmax, ms.xbuf[xp][hown]);
-                const float mx = (mraw > -INFINITY) ? mraw * (kF8 ? sl2h : sl2) : -INFINITY;
-                float corr = 1.f;
-                if (mx > -INFINITY) {
-                    if (m_ref == -INFINITY) {
-                        m_ref = mx;  // first visible tokens of the segment: nothing accumulated yet
-                        l = 0.f;
-                    } else if (kF8 ? (mx > m_ref + kRescaleLog2 ||
-                                      (mx < m_ref - kLowerLog2 && fmaxf(m_top, mx) - mx <= kMaxSpanLog2))
-                                   : mx > m_ref + kUpBf16) {
-                        corr = ex2_approx(m_ref - mx);  // < 1 up, > 1 down
-                        m_ref = mx;
-                        l *= corr;
-                        rescale = true;
-                    }
-                    m_top = fmaxf(m_top, mx);
-                }
-                ms.nb[hown] = (m_ref == -INFINITY) ? 0.f : (kF8 ? kPBias : 0.f) - m_ref;
-                ms.alpha[hown] = corr;
-                if (!ok) *abort_flag = 1;
-            }
-            const bool any_rescale = named_sync_or(kBarSm, kSmThreads, rescale);
-            if (*abort_flag) { alive = false; break; }
             // P^T is rewritten: the previous tile's P.V has read it (here and in the peer)
-            const bool pv_ok = wait_pv(ti - 1);
+            const bool pv_ok = ok && wait_pv(ti - 1);
             if (!pv_ok) *abort_flag = 1;
-            if (sm_tid == 0) mbar_arrive_expect_tx(&ms.p_in, kPRemote);  // the peer's half of this tile's P^T
-#pragma unroll
+            if (b_tid == 0) mbar_arrive_expect_tx(&ms.p_in, kPRemote);  // the peer's half of this tile's P^T
+            const uint32_t sbase = tm + 128u * sb + 64u * hh + lane_off;
+#pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 const int h0 = 64 * hh + 32 * c;
+                uint32_t r[32];
+                if (ok) {
+                    tmem_ld32(sbase + 32u * c, r);
+                    tmem_wait_ld();
+                }
                 float p[32];
-                const float4* nb4 = reinterpret_cast<const float4*>(&ms.nb[h0]);
-                const float4* sc4 = reinterpret_cast<const float4*>(&ms.sc[h0]);
+                const float4* nb4 = reinterpret_cast<const float4*>(&d.nb[h0]);
+                const float4* sc4 = reinterpret_cast<const float4*>(&d.sc[h0]);
 #pragma unroll
                 for (int k4 = 0; k4 < 8; ++k4) {
                     const float4 nb = nb4[k4];
-                    const float4 sc = kF8 ? sc4[k4] : make_float4(sl2, sl2, sl2, sl2);
+                    const float4 sc = sc4[k4];
                     float x[4];
-                    unpair_f32(fma_f32x2(pair_f32(sv[32 * c + 4 * k4], sv[32 * c + 4 * k4 + 1]), pair_f32(sc.x, sc.y),
-                                         pair_f32(nb.x, nb.y)),
+                    unpair_f32(fma_f32x2(pair_f32(__uint_as_float(r[4 * k4]), __uint_as_float(r[4 * k4 + 1])),
+                                         pair_f32(sc.x, sc.y), pair_f32(nb.x, nb.y)),
                                x[0], x[1]);
-                    unpair_f32(fma_f32x2(pair_f32(sv[32 * c + 4 * k4 + 2], sv[32 * c + 4 * k4 + 3]),
+                    unpair_f32(fma_f32x2(pair_f32(__uint_as_float(r[4 * k4 + 2]), __uint_as_float(r[4 * k4 + 3])),
                                          pair_f32(sc.z, sc.w), pair_f32(nb.z, nb.w)),
                                x[2], x[3]);
 #pragma unroll
@@ -735,24 +794,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 ms.red_sum[qw][h0 + lane] = xpose_reduce<false>(p);
             }
+            // S^T read by both groups: CTA 0 may compute the tile after next into it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(lead_sfree0 + 8u * sb);  // the loads were waited for
             if (p_local) fence_proxy_async_smem();  // this CTA's own P^T stores -> the MMA
             // O^T block hh, rows of lane quarter qw: columns of heads whose reference moved
             // (both CTAs apply the same factors to their rows)
-            if (any_rescale && pv_ok) {
+            if (d.rescale && pv_ok) {
 #pragma unroll 1
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t o0[32], o1[32];
-                    const uint32_t ta = tm + 256u + 128u * hh + 64u * hf + lane_off;
-                    tmem_ld32(ta, o0);
-                    tmem_ld32(ta + 32u, o1);
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t o[32];
+                    const uint32_t ta = tm + 256u + 128u * hh + 32u * ch + lane_off;
+                    tmem_ld32(ta, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        o0[k] = __float_as_uint(__uint_as_float(o0[k]) * ms.alpha[64 * hf + k]);
-                        o1[k] = __float_as_uint(__uint_as_float(o1[k]) * ms.alpha[64 * hf + 32 + k]);
-                    }
-                    tmem_st32(ta, o0);
-                    tmem_st32(ta + 32u, o1);
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * d.alpha[32 * ch + k]);
+                    tmem_st32(ta, o);
                 }
                 tmem_wait_st();
             }
@@ -765,15 +823,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (p_local) mbar_arrive(&ms.p_full);
                 else mbar_arrive_relaxed(&ms.p_full);
             }
-            named_sync(kBarSm, kSmThreads);
+            named_sync(kBarB, kSmThreads);
             if (*abort_flag) { alive = false; break; }
-            if (owner)
-                l += (ms.red_sum[0][hown] + ms.red_sum[1][hown]) + (ms.red_sum[2][hown] + ms.red_sum[3][hown]);
+            if (owner) {
+                l = l * d.alpha[hown] + (ms.red_sum[0][hown] + ms.red_sum[1][hown]) +
+                    (ms.red_sum[2][hown] + ms.red_sum[3][hown]);
+                m_fin = d.mref[hown];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.dec_free[sb]);  // group A may write this decision buffer again
             prev = t;
             ++ti;
         }
         if (alive && ti > 0) alive = epilogue(prev);
-        if (!alive && sm_tid == 0) raise_err(err, DCP_DEV_ERR_TIMEOUT);
+        if (!alive && b_tid == 0) raise_err(err, DCP_DEV_ERR_TIMEOUT);
     }
     __syncwarp();
     tc_fence_before();
@@ -807,7 +870,7 @@ template <bool kF8>
 cudaError_t launch_pair(const AttnArgs& a, cudaStream_t s) {
     const uint64_t qrows = (uint64_t)a.B * a.Tq * kHeads;
     const float* qscale = nullptr;
-    CUtensorMap tq, tqt, tkv;
+    CUtensorMap tq, tkv;
     if constexpr (kF8) {
         uint8_t* qp = a.ws + a.lay.off_qprep;
         float* qs = reinterpret_cast<float*>(qp + align256((size_t)qrows * mla_f8::kQRowBytes));
@@ -817,16 +880,13 @@ cudaError_t launch_pair(const AttnArgs& a, cudaStream_t s) {
                                    (int64_t)qrows, qp, qs);
         if (e != cudaSuccess) return e;
         if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, qp, mla_f8::kQRowBytes, qrows, mla_f8::kQRowBytes, 128, 64,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_map_2d(&tqt, CU_TENSOR_MAP_DATA_TYPE_UINT8, qp, mla_f8::kQRowBytes, qrows, mla_f8::kQRowBytes, 64, 64,
-                         CU_TENSOR_MAP_SWIZZLE_64B))
+                         CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         qscale = qs;
     } else {
         if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kDk, qrows, kDk * 2, 64, 64,
                          CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        tqt = tq;  // unused
     }
     const uint64_t rows = (uint64_t)a.num_blocks * a.bs;
     if (rows + kChunk > 0x7FFFFFFFull) return cudaErrorInvalidValue;  // row coordinates are int32
@@ -836,7 +896,7 @@ cudaError_t launch_pair(const AttnArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(mla_pair_kernel<kF8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(2 * a.W), (unsigned)a.Tq);
-    return launch_pdl(mla_pair_kernel<kF8>, grid, dim3(kThreads), kSmem, s, a, tq, tqt, tkv, qscale);
+    return launch_pdl(mla_pair_kernel<kF8>, grid, dim3(kThreads), kSmem, s, a, tq, tkv, qscale);
 }
 
 }  // namespace
