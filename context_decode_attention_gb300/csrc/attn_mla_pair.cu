@@ -71,7 +71,7 @@ using namespace mla;
 constexpr int kTileCh = 4;             // chunks per pair tile (256 tokens)
 constexpr int kBox = 8192;             // one TMA box: 64 rows x 128 bytes
 constexpr int kSlot = 2 * kBox;        // ring slot: 128 rows x 128 bytes
-constexpr int kRing = 7;
+constexpr int kRing = 7;               // ring slots, at most (bf16 7, FP8 5)
 constexpr int kProd = 3;
 constexpr int kWarpMma = kProd;
 constexpr int kWarpSm = kWarpMma + 1;
@@ -85,13 +85,12 @@ constexpr int kQBytes = 9 * kBox;      // this CTA's 64 query rows x 1152 bytes
 constexpr int kOffP = kQBytes;
 constexpr int kPBytes = 4 * kBox;      // P^T: 256 tokens x 64 heads (bf16, or e4m3 hi + lo)
 constexpr uint32_t kPRemote = kPBytes / 2;  // the part of P^T the peer's 128 tokens write
-constexpr int kOffRing = kOffP + kPBytes;
-constexpr int kOffMisc = kOffRing + kRing * kSlot;
+constexpr int kOffMisc = kOffP + kPBytes + kRing * kSlot;  // the same for both layouts (Cfg)
 constexpr int kUnits = 64;
 constexpr int kTileRing = 8;
 constexpr int kBarA = 1;               // named barriers of the two softmax groups
 constexpr int kBarB = 2;
-static_assert(kOffP % 1024 == 0 && kOffRing % 1024 == 0, "swizzled operands need 1024-byte alignment");
+static_assert(kOffP % 1024 == 0, "swizzled operands need 1024-byte alignment");
 static_assert(kUnits <= kUnitCache, "unit cache");
 
 // Softmax references (log2 units).  bf16: p' = 2^(x - m_ref), the reference
@@ -124,7 +123,10 @@ struct Decision {
 
 struct Misc {
     uint64_t full[kRing], empty[kRing];
-    uint64_t q_full, q_empty, s_full[2], s_free[2], p_full, p_free, p_in, p_peer, xmax[2], xl, drain;
+    uint64_t q_full, q_empty, s_full[2], s_free[2], xmax[2], xl, drain;
+    // per tile parity: a tile's P^T complete here (group B), the peer's part of it
+    // landed here, CTA 1's complete (forwarded), its P.V done
+    uint64_t p_full[2], p_in[2], p_peer[2], p_free[2];
     uint64_t dec_full[2], dec_free[2];
     uint32_t tmem_slot;
     int32_t abort;
@@ -145,6 +147,9 @@ template <bool kF8>
 struct Cfg;
 template <>
 struct Cfg<false> {                    // bf16 cache
+    static constexpr int kPBufs = 1;   // P^T buffers
+    static constexpr int kRingN = 7;   // ring slots
+    static constexpr int kAhead = 1;   // QK(i + 1) is issued before P.V(i)
     static constexpr int kKItems = 9;  // K sub-tiles of 64 columns
     static constexpr int kVItems = 8;  // V^T items (block b, chunk k): 128 values x 64 tokens
     static constexpr int kCols = 64;   // elements per 128-byte box row
@@ -153,6 +158,12 @@ struct Cfg<false> {                    // bf16 cache
 };
 template <>
 struct Cfg<true> {                     // e4m3 cache
+    // two P^T buffers, so that group B never waits for the previous tile's P.V
+    // before storing, and QK runs two tiles ahead of P.V (fewer items per tile:
+    // five ring slots keep the cache stream going)
+    static constexpr int kPBufs = 2;
+    static constexpr int kRingN = 5;
+    static constexpr int kAhead = 2;
     static constexpr int kKItems = 5;  // K sub-tiles of 128 columns (the last: 512-575, then zeros)
     static constexpr int kVItems = 4;  // V^T items (block b, token half h): 128 values x 128 tokens
     static constexpr int kCols = 128;
@@ -228,7 +239,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
     uint8_t* const sQ = smem;
     uint8_t* const sP = smem + kOffP;
-    uint8_t* const sRing = smem + kOffRing;
+    uint8_t* const sRing = smem + kOffP + C::kPBufs * kPBytes;
+    static_assert(kOffP + C::kPBufs * kPBytes + C::kRingN * kSlot <= kOffMisc, "ring");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t cta = cluster_rank();  // CTA 0 issues the pair's MMAs
@@ -251,7 +263,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int64_t ncache = cache_units(ms.units, us, a.U, u0, kUnits);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kRing; ++i) {
+        for (int i = 0; i < C::kRingN; ++i) {
             mbar_init(&ms.full[i], 1);
             mbar_init(&ms.empty[i], 1);
         }
@@ -263,11 +275,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(&ms.xmax[i], 1);
             mbar_init(&ms.dec_full[i], kAWarps);     // group A
             mbar_init(&ms.dec_free[i], kSmWarps);    // group B
+            mbar_init(&ms.p_full[i], kSmWarps);      // this CTA's group B
+            mbar_init(&ms.p_free[i], 1);
+            mbar_init(&ms.p_in[i], 1);
+            mbar_init(&ms.p_peer[i], 1);
         }
-        mbar_init(&ms.p_full, kSmWarps);  // this CTA's group B
-        mbar_init(&ms.p_free, 1);
-        mbar_init(&ms.p_in, 1);
-        mbar_init(&ms.p_peer, 1);
         mbar_init(&ms.xl, 1);
         mbar_init(&ms.drain, 1);
         ms.abort = 0;
@@ -295,7 +307,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const int me = warp;
             Ring ring;
-            ring.n = kRing;
+            ring.n = C::kRingN;
             uint32_t qe_phase = 0;
             bool alive = true, bad_block = false;
             const int oob_row = (int)((int64_t)a.num_blocks * a.bs);  // a box from here reads zeros
@@ -344,8 +356,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 ring.advance();
             };
-            Ahead cur_t, nxt, prev;
-            prev.valid = false;
+            // the V^T items of tile p: after the K items of tile p + kAhead (the order in
+            // which the MMA issuer consumes them)
+            auto load_v = [&](const Ahead& pt) {
+                const int x = 128 * (int)cta;
+                if constexpr (!kF8) {
+                    for (int bb = 0; bb < 2 && alive; ++bb)
+                        for (int k = 0; k < kTileCh && alive; ++k) {
+                            const int y = row_of(pt, k);
+                            item(256 * bb + x, y, 256 * bb + x + 64, y);
+                        }
+                } else {
+                    for (int bb = 0; bb < 2 && alive; ++bb)
+                        for (int hh = 0; hh < 2 && alive; ++hh)
+                            item(256 * bb + x, row_of(pt, 2 * hh), 256 * bb + x, row_of(pt, 2 * hh + 1));
+                }
+            };
+            Ahead cur_t, nxt, p1, p2;
+            p1.valid = p2.valid = false;
             fetch(cur_t);
             int ti = 0;
             for (;;) {
@@ -380,22 +408,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int ya = row_of(cur_t, 2 * (int)cta), yb = row_of(cur_t, 2 * (int)cta + 1);
                     for (int s = 0; s < C::kKItems && alive; ++s) item(C::kCols * s, ya, C::kCols * s, yb);
                 }
-                if (prev.valid) {
-                    const int x = 128 * (int)cta;
-                    if constexpr (!kF8) {
-                        for (int bb = 0; bb < 2 && alive; ++bb)
-                            for (int k = 0; k < kTileCh && alive; ++k) {
-                                const int y = row_of(prev, k);
-                                item(256 * bb + x, y, 256 * bb + x + 64, y);
-                            }
-                    } else {
-                        for (int bb = 0; bb < 2 && alive; ++bb)
-                            for (int hh = 0; hh < 2 && alive; ++hh)
-                                item(256 * bb + x, row_of(prev, 2 * hh), 256 * bb + x, row_of(prev, 2 * hh + 1));
-                    }
+                const Ahead& pt = C::kAhead == 2 ? p2 : p1;
+                if (pt.valid) load_v(pt);
+                if (!cur_t.valid) {
+                    if (C::kAhead == 2 && p1.valid) load_v(p1);  // the last tile's values
+                    break;
                 }
-                if (!cur_t.valid || !alive) break;
-                prev = cur_t;
+                if (!alive) break;
+                p2 = p1;
+                p1 = cur_t;
                 cur_t = nxt;
                 ++ti;
             }
@@ -409,8 +430,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer (CTA 0, one thread)
         if (cta == 0 && lane == 0) {
             Ring ring;
-            ring.n = kRing;
-            uint32_t qf_phase = 0, sfree_phase[2] = {0u, 0u}, pfull_phase = 0;
+            ring.n = C::kRingN;
+            uint32_t qf_phase = 0, sfree_phase[2] = {0u, 0u};
             bool alive = true, more = true;
             // descriptors (start address in 16-byte units in the low bits)
             const uint64_t dq = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSW128);
@@ -421,18 +442,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t dp = kF8 ? smem_desc(smem_u32(sP), 16, 512, kLayoutSW64)
                                     : smem_desc(smem_u32(sP), 16, 1024, kLayoutSW128);
             constexpr uint32_t kSlotD = kSlot >> 4, kBoxD = kBox >> 4;
-            TileMsg prev{}, t{};
-            int ti = 0;
+            // QK of tile j is issued while j <= (oldest pending P.V) + kAhead: QK(j) needs only
+            // that group B has loaded S^T(j - 2), which it does before its stores
+            TileMsg hist[4];
+            int qk = 0, pv = 0;
             for (;;) {
-                if (more) {
+                while (alive && more && qk <= pv + C::kAhead) {
                     if (!mbar_wait_sleep(&ms.full[ring.slot], ring.phase)) { alive = false; break; }
-                    t = ms.tmsg[ti % kTileRing];
+                    const TileMsg t = ms.tmsg[qk % kTileRing];
+                    hist[qk & 3] = t;
                     if (t.first) {
                         if (!mbar_wait_sleep(&ms.q_full, qf_phase)) { alive = false; break; }
                         qf_phase ^= 1u;
                     }
-                    const int sb = ti & 1;  // S^T double buffer
-                    if (ti >= 2) {  // both CTAs' group B has read the buffer's previous tile
+                    const int sb = qk & 1;  // S^T double buffer
+                    if (qk >= 2) {  // both CTAs' group B has read the buffer's previous tile
                         if (!mbar_wait_sleep_cluster(&ms.s_free[sb], sfree_phase[sb])) { alive = false; break; }
                         sfree_phase[sb] ^= 1u;
                     }
@@ -466,48 +490,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (!alive) break;
                     mma_commit_pair(&ms.s_full[sb]);
                     if (t.last) mma_commit_pair(&ms.q_empty);
+                    more = t.has_next != 0;
+                    ++qk;
                 }
-                if (ti > 0) {
-                    // O^T += V^T P^T of the previous tile, once P^T is complete in both CTAs: this
-                    // CTA's group B (its stores here, its O^T rescale), the part CTA 1 sent here,
-                    // and CTA 1's own (forwarded by its warp 3)
-                    const TileMsg pt = prev;
-                    if (!mbar_wait_sleep(&ms.p_full, pfull_phase) || !mbar_wait_sleep_cluster(&ms.p_in, pfull_phase) ||
-                        !mbar_wait_sleep_cluster(&ms.p_peer, pfull_phase)) { alive = false; break; }
-                    pfull_phase ^= 1u;
+                if (!alive || pv == qk) break;
+                // O^T += V^T P^T of tile pv, once P^T is complete in both CTAs: this CTA's
+                // group B (its stores here, its O^T rescale), the part CTA 1 sent here, and
+                // CTA 1's own (forwarded by its warp 3)
+                const TileMsg pt = hist[pv & 3];
+                const int pq = pv & 1;
+                const uint32_t pph = (uint32_t)((pv >> 1) & 1);
+                if (!mbar_wait_sleep(&ms.p_full[pq], pph) || !mbar_wait_sleep_cluster(&ms.p_in[pq], pph) ||
+                    !mbar_wait_sleep_cluster(&ms.p_peer[pq], pph)) { alive = false; break; }
+                const uint64_t dpb = dp + (uint64_t)((C::kPBufs == 2 ? (pv & 1) : 0) * (kPBytes >> 4));
 #pragma unroll 1
-                    for (int it = 0; it < C::kVItems; ++it) {
-                        if (!mbar_wait_sleep(&ms.full[ring.slot], ring.phase)) { alive = false; break; }
-                        tc_fence_after();
-                        const uint64_t va = dv + ring.slot * kSlotD;
-                        if constexpr (!kF8) {
-                            const int bb = it >> 2, k = it & 3;
-                            const uint32_t o = tm + 256u + 128u * bb;
+                for (int it = 0; it < C::kVItems; ++it) {
+                    if (!mbar_wait_sleep(&ms.full[ring.slot], ring.phase)) { alive = false; break; }
+                    tc_fence_after();
+                    const uint64_t va = dv + ring.slot * kSlotD;
+                    if constexpr (!kF8) {
+                        const int bb = it >> 2, k = it & 3;
+                        const uint32_t o = tm + 256u + 128u * bb;
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_pair_f16(o, va + kk * (2048 >> 4), dp + (64 * k + 16 * kk) * (128 >> 4), C::kIdescPV,
-                                             !(pt.first && k == 0 && kk == 0));
-                        } else {
-                            const int bb = it >> 1, hh = it & 1;
-                            const uint32_t o = tm + 256u + 128u * bb;
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_pair_f16(o, va + kk * (2048 >> 4), dpb + (64 * k + 16 * kk) * (128 >> 4), C::kIdescPV,
+                                         !(pt.first && k == 0 && kk == 0));
+                    } else {
+                        const int bb = it >> 1, hh = it & 1;
+                        const uint32_t o = tm + 256u + 128u * bb;
 #pragma unroll 1
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint32_t tok = 128 * hh + 32 * kk;
-                                mma_pair_f8(o, va + kk * (4096 >> 4), dp + tok * (64 >> 4), C::kIdescPV,
-                                            !(pt.first && hh == 0 && kk == 0));
-                                mma_pair_f8(o, va + kk * (4096 >> 4), dp + (16384 >> 4) + tok * (64 >> 4), C::kIdescPV, 1u);
-                            }
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t tok = 128 * hh + 32 * kk;
+                            mma_pair_f8(o, va + kk * (4096 >> 4), dpb + tok * (64 >> 4), C::kIdescPV,
+                                        !(pt.first && hh == 0 && kk == 0));
+                            mma_pair_f8(o, va + kk * (4096 >> 4), dpb + (16384 >> 4) + tok * (64 >> 4), C::kIdescPV,
+                                        1u);
                         }
-                        mma_commit_pair(&ms.empty[ring.slot]);
-                        ring.advance();
                     }
-                    if (!alive) break;
-                    mma_commit_pair(&ms.p_free);
+                    mma_commit_pair(&ms.empty[ring.slot]);
+                    ring.advance();
                 }
-                if (!more) break;
-                more = t.has_next != 0;
-                prev = t;
-                ++ti;
+                if (!alive) break;
+                mma_commit_pair(&ms.p_free[pq]);
+                ++pv;
             }
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
             // every MMA of the pair completes before either CTA releases tensor memory
@@ -518,14 +543,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // here, their O^T rescale) and CTA 0's part of its P^T has landed here, one
             // release at cluster scope to the MMA issuer (the softmax threads then never
             // release at cluster scope behind their own outstanding remote stores)
-            const uint32_t lead_ppeer = mapa_shared(smem_u32(&ms.p_peer), 0);
+            const uint32_t lead_ppeer0 = mapa_shared(smem_u32(&ms.p_peer[0]), 0);
             Tile tt;
-            uint32_t ph = 0;
+            int i = 0;
             bool alive = true;
             while (alive && cur.next(tt)) {
-                if (!mbar_wait_sleep(&ms.p_full, ph) || !mbar_wait_sleep_cluster(&ms.p_in, ph)) { alive = false; break; }
-                ph ^= 1u;
-                mbar_arrive_cluster(lead_ppeer);
+                const uint32_t ph = (uint32_t)((i >> 1) & 1);
+                if (!mbar_wait_sleep(&ms.p_full[i & 1], ph) || !mbar_wait_sleep_cluster(&ms.p_in[i & 1], ph)) {
+                    alive = false;
+                    break;
+                }
+                mbar_arrive_cluster(lead_ppeer0 + 8u * (i & 1));
+                ++i;
             }
             if (!alive) raise_err(err, DCP_DEV_ERR_TIMEOUT);
         }
@@ -656,11 +685,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t lead_sfree0 = mapa_shared(smem_u32(&ms.s_free[0]), 0);
         const uint32_t peer_lbuf = mapa_shared(smem_u32(&ms.lbuf[0]), peer);
         const uint32_t peer_xl = mapa_shared(smem_u32(&ms.xl), peer);
-        const uint32_t peer_pin = mapa_shared(smem_u32(&ms.p_in), peer);
+        const uint32_t peer_pin0 = mapa_shared(smem_u32(&ms.p_in[0]), peer);
         // this warp's P^T columns live in CTA hh; this token's row and its swizzle
         // (SW128 rows of 128 bytes, SW64 rows of 64 bytes)
         const bool p_local = hh == (int)cta;
-        const uint32_t p_base = p_local ? smem_u32(sP) : mapa_shared(smem_u32(sP), peer);
+        const uint32_t p_base0 = p_local ? smem_u32(sP) : mapa_shared(smem_u32(sP), peer);
         const uint32_t prow = kF8 ? (uint32_t)jrow * 64u : (uint32_t)jrow * 128u;
         const uint32_t pswz = kF8 ? (uint32_t)((jrow >> 1) & 3) : (uint32_t)(jrow & 7);
         volatile int32_t* abort_flag = &ms.abort;
@@ -670,7 +699,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto wait_pv = [&](int k) -> bool {
             if (k < 0 || pv_done >= k) return true;
             // warp-uniform outcome: TMEM loads and stores follow under it
-            if (!__all_sync(0xffffffffu, mbar_wait(&ms.p_free, (uint32_t)(k & 1)))) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(&ms.p_free[k & 1], (uint32_t)((k >> 1) & 1)))) return false;
             pv_done = k;
             tc_fence_after();
             return true;
@@ -734,10 +763,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const Decision& d = ms.dec[sb];
             const bool vis = ok && jrow < kChunk * t.n_ch && t.chunk * kChunk + jrow < bound;
-            // P^T is rewritten: the previous tile's P.V has read it (here and in the peer)
-            const bool pv_ok = ok && wait_pv(ti - 1);
+            // P^T buffer of this tile: its previous user's P.V (tile ti - kPBufs) has read it,
+            // here and in the peer
+            const uint32_t p_base = p_base0 + (uint32_t)((C::kPBufs == 2 ? (ti & 1) : 0) * kPBytes);
+            bool pv_ok = ok && wait_pv(ti - C::kPBufs);
             if (!pv_ok) *abort_flag = 1;
-            if (b_tid == 0) mbar_arrive_expect_tx(&ms.p_in, kPRemote);  // the peer's half of this tile's P^T
+            if (b_tid == 0) mbar_arrive_expect_tx(&ms.p_in[ti & 1], kPRemote);  // the peer's half of this tile's P^T
+            const uint32_t peer_pin = peer_pin0 + 8u * (ti & 1);
             const uint32_t sbase = tm + 128u * sb + 64u * hh + lane_off;
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
@@ -800,7 +832,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive_cluster_relaxed(lead_sfree0 + 8u * sb);  // the loads were waited for
             if (p_local) fence_proxy_async_smem();  // this CTA's own P^T stores -> the MMA
             // O^T block hh, rows of lane quarter qw: columns of heads whose reference moved
-            // (both CTAs apply the same factors to their rows)
+            // (both CTAs apply the same factors to their rows), once O^T holds tile ti - 1
+            if (d.rescale && pv_ok) {
+                pv_ok = wait_pv(ti - 1);
+                if (!pv_ok) *abort_flag = 1;
+            }
             if (d.rescale && pv_ok) {
 #pragma unroll 1
                 for (int ch = 0; ch < 4; ++ch) {
@@ -820,8 +856,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // sent to the peer, tracked there by its receive barrier) only order their O^T
             // rescale, already waited for
             if (lane == 0) {
-                if (p_local) mbar_arrive(&ms.p_full);
-                else mbar_arrive_relaxed(&ms.p_full);
+                if (p_local) mbar_arrive(&ms.p_full[ti & 1]);
+                else mbar_arrive_relaxed(&ms.p_full[ti & 1]);
             }
             named_sync(kBarB, kSmThreads);
             if (*abort_flag) { alive = false; break; }
