@@ -48,6 +48,10 @@ def load_peaks():
 # the launch's cached tokens; summaries and commands under profiles/).  Valid
 # only for the kernel source they were taken on: a changed source gives null.
 MEASURED_TRAFFIC = {
+    ("mla_tcgen05", "fp8"): ("attn_mla_pair.cu", "ed0a7ad240eeb1855500b6a29b9cb437ae195f2d4ae1468c54e9b997a7c05a1f",
+                             (219.654656e6 + 4.898048e6) / 376734),
+    ("mla_tcgen05", "bf16"): ("attn_mla_pair.cu", "ed0a7ad240eeb1855500b6a29b9cb437ae195f2d4ae1468c54e9b997a7c05a1f",
+                              (308.060416e6 + 6.346240e6) / 262144),
     ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "55f1cce0d8111ec459e79dfdc0f0496849629421f35c1b418f54f7e664fe62df",
                           (268.632576e6 + 3.230976e6) / 65536),
     # per table entry (N B max_blocks) of the block-transfer listing
