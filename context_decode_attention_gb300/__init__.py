@@ -8,7 +8,8 @@ back to the CPU: if the library is missing or cannot load, every call raises.
 Functions carry the C ABI's names (include/dcp.h):
   dcp_workspace_size, dcp_workspace_init, dcp_get_error, dcp_slot_mapping, dcp_transfer_blocks, dcp_pcp_partition, dcp_prefill_attention,
   dcp_sparse_workspace_size, dcp_sparse_localize, dcp_sparse_decode_attention,
-  dcp_partial_attention, dcp_lse_merge, dcp_decode_attention, dcp_decode_attention_noalloc,
+  dcp_partial_attention, dcp_lse_merge, dcp_decode_attention, dcp_decode_plan, dcp_decode_attention_planned,
+  dcp_decode_attention_noalloc,
   dcp_noalloc_get_error
 """
 
@@ -24,7 +25,8 @@ __all__ = [
     "DcpError", "DcpParams", "params_from_config", "lib", "lib_path",
     "dcp_workspace_size", "dcp_workspace_init", "dcp_get_error", "dcp_slot_mapping", "dcp_transfer_blocks", "dcp_pcp_partition",
     "dcp_prefill_attention", "dcp_sparse_workspace_size", "dcp_sparse_localize", "dcp_sparse_decode_attention",
-    "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention", "dcp_decode_attention_noalloc",
+    "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention", "dcp_decode_plan",
+    "dcp_decode_attention_planned", "dcp_decode_attention_noalloc",
     "dcp_noalloc_get_error", "dcp_launch_count",
     "dcp_attention_kernel", "DCP_F32", "DCP_BF16", "DCP_FP8_E4M3", "DCP_LAYOUT_GQA", "DCP_LAYOUT_MLA",
 ]
@@ -297,6 +299,31 @@ def dcp_decode_attention(params, q, k_pool, v_pool, num_blocks, block_tables, se
                                       int(block_tables.shape[-1]), _ptr(seq_lens), _ptr(local_lens),
                                       _ptr(out), _ptr(lse), _ptr(workspace), _nbytes(workspace),
                                       _stream(stream)), "dcp_decode_attention")
+
+
+def dcp_decode_plan(params, seq_lens, local_lens, max_blocks, workspace, stream=None):
+    """The work plan of dcp_decode_attention_planned, made ahead (include/dcp.h):
+    it depends on the lengths only, so it can run beside the step's cache write
+    or once for every layer of a step."""
+    B = int(seq_lens.numel())
+    _need(seq_lens, "seq_lens", B * 4, 4)
+    _need(local_lens, "local_lens", params.N * B * 4, 4)
+    _check(lib().dcp_decode_plan(ctypes.byref(params), B, _ptr(seq_lens), _ptr(local_lens), int(max_blocks),
+                                 _ptr(workspace), _nbytes(workspace), _stream(stream)), "dcp_decode_plan")
+
+
+def dcp_decode_attention_planned(params, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens,
+                                 out, lse, workspace, stream=None):
+    """dcp_decode_attention on the plan dcp_decode_plan left in the workspace
+    (same arguments; a plan for other arguments raises DCP_DEV_ERR_PLAN)."""
+    B = int(seq_lens.numel())
+    rows = _need_attention(params, B, q, k_pool, v_pool, num_blocks, block_tables, seq_lens, local_lens)
+    _need_decode_out(params, rows, out, lse)
+    _check(lib().dcp_decode_attention_planned(ctypes.byref(params), B, _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                              int(num_blocks), _ptr(block_tables), int(block_tables.shape[-1]),
+                                              _ptr(seq_lens), _ptr(local_lens), _ptr(out), _ptr(lse),
+                                              _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "dcp_decode_attention_planned")
 
 
 def dcp_lse_merge(N, rows, Dv, out_partial, lse_partial, out, out_dtype, lse=None, stream=None):

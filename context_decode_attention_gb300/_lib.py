@@ -13,7 +13,7 @@ DCP_LAYOUT_GQA, DCP_LAYOUT_MLA = 0, 1
 EXPORTS = [
     "dcp_version", "dcp_error_string", "dcp_launch_count", "dcp_attention_kernel", "dcp_workspace_size", "dcp_workspace_init", "dcp_get_error",
     "dcp_slot_mapping", "dcp_transfer_blocks", "dcp_pcp_partition", "dcp_prefill_attention",
-    "dcp_sparse_workspace_size", "dcp_sparse_localize", "dcp_sparse_decode_attention", "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention",
+    "dcp_sparse_workspace_size", "dcp_sparse_localize", "dcp_sparse_decode_attention", "dcp_partial_attention", "dcp_lse_merge", "dcp_decode_attention", "dcp_decode_plan", "dcp_decode_attention_planned",
     "dcp_decode_attention_noalloc", "dcp_noalloc_get_error",
 ]
 
@@ -71,6 +71,8 @@ def lib():
         "dcp_partial_attention": (ctypes.c_int, [P, i32, p, p, p, i64, p, i32, p, p, p, p, p, sz, p]),
         "dcp_lse_merge": (ctypes.c_int, [i32, i64, i32, p, p, p, i32, p, p]),
         "dcp_decode_attention": (ctypes.c_int, [P, i32, p, p, p, i64, p, i32, p, p, p, p, p, sz, p]),
+        "dcp_decode_plan": (ctypes.c_int, [P, i32, p, p, i32, p, sz, p]),
+        "dcp_decode_attention_planned": (ctypes.c_int, [P, i32, p, p, p, i64, p, i32, p, p, p, p, p, sz, p]),
         "dcp_decode_attention_noalloc": (ctypes.c_int, [P, i32, p, p, p, i64, p, i32, p, p, p, p, p]),
         "dcp_noalloc_get_error": (ctypes.c_int, [p, ctypes.POINTER(ctypes.c_uint32)]),
     }

@@ -24,6 +24,10 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(AttnArgs a, int q_dty
     pdl_trigger();  // the segment merge may launch
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(a.ws);
     const int64_t P = hdr->total_chunks;
+    if (hdr->plan_key != a.plan_key) {  // the workspace holds a plan for other arguments
+        if (threadIdx.x == 0) raise_err(&reinterpret_cast<WsHeader*>(a.ws)->err, DCP_DEV_ERR_PLAN);
+        return;
+    }
     if (P == 0) return;
     const int64_t w = blockIdx.x;
     const int64_t We = P < a.W ? P : a.W;  // workers in play: each owns >= 1 chunk

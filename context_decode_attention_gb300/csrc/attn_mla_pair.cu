@@ -50,9 +50,10 @@
 //   warps 8-15  ... while group B computes tile i's probabilities, P^T, row
 //               sums, O^T rescale and segment epilogue (thread = TMEM lane;
 //               two warps per lane quarter, one per half of the heads)
-// Shared memory: query half 72 KB | P^T 32 KB | ring of seven 16 KB slots.
-// TMEM (512 columns per CTA): S^T in [0, 256) (bf16: two buffers of 128
-// columns; FP8: one buffer, hi then lo), O^T blocks [256, 384) and [384, 512).
+// Shared memory: query half 72 KB | P^T 32 KB (FP8: two buffers) | ring of
+// 16 KB slots (bf16 seven, FP8 five).
+// TMEM (512 columns per CTA): S^T buffers [0, 128) and [128, 256), O^T blocks
+// [256, 384) and [384, 512).
 // Every wait is bounded; a timeout sets DCP_DEV_ERR_TIMEOUT and the role stops
 // (the softmax warps leave together, through a flag read after each of their
 // barriers).
@@ -250,6 +251,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     pdl_trigger();                        // the segment merge may launch
     uint32_t* err = &reinterpret_cast<WsHeader*>(a.ws)->err;
     const int64_t P = reinterpret_cast<const WsHeader*>(a.ws)->total_chunks;
+    if (reinterpret_cast<const WsHeader*>(a.ws)->plan_key != a.plan_key) {  // a plan for other arguments
+        if (threadIdx.x == 0) raise_err(err, DCP_DEV_ERR_PLAN);
+        return;                                                              // (every CTA: same header)
+    }
     if (P == 0) return;
     const int64_t We = P < a.W ? P : a.W;
     if (w >= We) return;                  // both CTAs of the pair leave here together
@@ -259,7 +264,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     const int64_t c0 = worker_begin(w, We, P), c1 = worker_begin(w + 1, We, P);
     const int64_t* us = reinterpret_cast<const int64_t*>(a.ws + a.lay.off_units);
-    const int64_t u0 = unit_of_chunk(us, a.U, c0);
+    const int64_t u0 = a.worker_starts ? reinterpret_cast<const WorkerStart*>(a.ws + a.lay.off_wfirst)[w].u0
+                                       : unit_of_chunk(us, a.U, c0);
     const int64_t ncache = cache_units(ms.units, us, a.U, u0, kUnits);
 
     if (threadIdx.x == 0) {

@@ -98,29 +98,62 @@ bool layout_for(const dcp_params& p, int32_t B, WsLayout* out, Kernel* kout, int
     const int64_t w = k == Kernel::kNone ? 0 : kernel_workers(k, sms, p);
     const int64_t rows = (int64_t)p.Tq * (p.Hq / p.Hkv);
     const size_t qprep = (k == Kernel::kMlaTc && p.kv_dtype == DCP_FP8_E4M3) ? mla_f8_qprep_bytes(B, p.Tq) : 0;
-    *out = ws_layout(U, U, w + U, rows, p.Dv, qprep);
+    *out = ws_layout(U, U, w + U, rows, p.Dv, qprep, w);
     if (kout) *kout = k;
     if (W) *W = w;
     return true;
+}
+
+// Where the work plan of an attention call is made.
+enum class PlanMode {
+    kInline,   // the planner launches just before the kernels (PDL overlaps their launch)
+    kOnly,     // a plan made ahead (dcp_decode_plan): the planner alone, with worker starts
+    kPlanned,  // the kernels alone, on a plan made ahead with the same arguments
+};
+
+// The arguments a plan depends on, folded into 64 bits (FNV-1a).  Written by
+// the planner into the workspace header; every attention kernel compares it
+// with its own and refuses a plan made for other arguments.  Never 0 (a
+// zeroed workspace holds no plan).
+uint64_t plan_key_of(const dcp_params& p, int32_t B, int32_t max_blocks, const int32_t* seq_lens,
+                     const int32_t* local_lens, bool partial_mode, bool lens_given, bool worker_starts, int64_t W,
+                     int CH) {
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&](uint64_t v) {
+        for (int i = 0; i < 8; ++i) {
+            h ^= (v >> (8 * i)) & 0xffu;
+            h *= 1099511628211ull;
+        }
+    };
+    const int64_t f[] = {p.layout, p.N, p.I, p.block_size, p.Hq, p.Hkv, p.Dk, p.Dv, p.Tq, p.q_dtype, p.kv_dtype,
+                         B, max_blocks, partial_mode, lens_given, worker_starts, W, CH};
+    for (int64_t v : f) mix((uint64_t)v);
+    mix((uint64_t)reinterpret_cast<uintptr_t>(seq_lens));
+    mix((uint64_t)reinterpret_cast<uintptr_t>(local_lens));
+    return h | 1u;
 }
 
 int run_attention(const dcp_params* params, int32_t B, const void* q, const void* k_pool,
                   const void* v_pool, int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks,
                   const int32_t* seq_lens, const int32_t* local_lens, bool partial_mode, float* out_partial,
                   float* lse_partial, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                  cudaStream_t stream, bool lens_given = false) {
+                  cudaStream_t stream, bool lens_given = false, PlanMode mode = PlanMode::kInline) {
     int rc = validate_params(params);
     if (rc != DCP_OK) return rc;
     const dcp_params& p = *params;
     if (B < 0) return DCP_ERR_INVALID_ARG;
     if (B == 0) return DCP_OK;
-    if (!q || !k_pool || !block_tables || !seq_lens || !local_lens) return DCP_ERR_INVALID_ARG;
-    if (p.layout == DCP_LAYOUT_GQA && !v_pool) return DCP_ERR_INVALID_ARG;
-    if (p.layout == DCP_LAYOUT_MLA && v_pool) return DCP_ERR_INVALID_ARG;
-    if (partial_mode && (!out_partial || !lse_partial)) return DCP_ERR_INVALID_ARG;
-    if (!partial_mode && !out) return DCP_ERR_INVALID_ARG;
-    if (num_blocks < 1 || max_blocks < 1) return DCP_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_pool) || (v_pool && !aligned16(v_pool))) return DCP_ERR_INVALID_ARG;
+    if (!seq_lens || !local_lens) return DCP_ERR_INVALID_ARG;
+    if (max_blocks < 1) return DCP_ERR_INVALID_ARG;
+    if (mode != PlanMode::kOnly) {
+        if (!q || !k_pool || !block_tables) return DCP_ERR_INVALID_ARG;
+        if (p.layout == DCP_LAYOUT_GQA && !v_pool) return DCP_ERR_INVALID_ARG;
+        if (p.layout == DCP_LAYOUT_MLA && v_pool) return DCP_ERR_INVALID_ARG;
+        if (partial_mode && (!out_partial || !lse_partial)) return DCP_ERR_INVALID_ARG;
+        if (!partial_mode && !out) return DCP_ERR_INVALID_ARG;
+        if (num_blocks < 1) return DCP_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k_pool) || (v_pool && !aligned16(v_pool))) return DCP_ERR_INVALID_ARG;
+    }
     if (!workspace) return DCP_ERR_WORKSPACE;
     WsLayout lay;
     Kernel kern;
@@ -128,6 +161,7 @@ int run_attention(const dcp_params* params, int32_t B, const void* q, const void
     if (!layout_for(p, B, &lay, &kern, &W)) return DCP_ERR_CUDA;
     if (kern == Kernel::kNone) return DCP_ERR_UNSUPPORTED;
     if (workspace_bytes < lay.total) return DCP_ERR_WORKSPACE;
+    const bool ahead = mode != PlanMode::kInline;  // the plan holds each worker's first unit
 
     AttnArgs a;
     memset(&a, 0, sizeof a);
@@ -135,23 +169,28 @@ int run_attention(const dcp_params* params, int32_t B, const void* q, const void
     a.Tq = p.Tq; a.G = p.Hq / p.Hkv; a.B = B; a.max_blocks = max_blocks; a.layout = p.layout;
     a.partial_mode = partial_mode ? 1 : 0; a.out_dtype = p.out_dtype; a.CH = kernel_chunk(kern, p);
     a.num_blocks = num_blocks; a.U = (int64_t)B * p.Hkv * p.N;
+    if (a.U >= (int64_t)1 << 31) return DCP_ERR_INVALID_ARG;  // unit ids are 32-bit in the plan
     a.Gn = partial_mode ? a.U : (int64_t)B * p.Hkv; a.W = W;
     a.softmax_scale = p.softmax_scale; a.kv_scale = p.kv_scale;
     a.q = q; a.k_pool = k_pool; a.v_pool = v_pool; a.block_tables = block_tables; a.seq_lens = seq_lens;
     a.local_lens = local_lens; a.out_partial = out_partial; a.lse_partial = lse_partial; a.out = out;
     a.lse = lse; a.ws = reinterpret_cast<uint8_t*>(workspace); a.lay = lay; a.rows = p.Tq * a.G;
     a.lens_given = lens_given ? 1 : 0;
+    a.worker_starts = ahead ? 1 : 0;
+    a.plan_key = plan_key_of(p, B, max_blocks, seq_lens, local_lens, partial_mode, lens_given, ahead, W, a.CH);
 
-    PlanArgs pa;
-    memset(&pa, 0, sizeof pa);
-    pa.N = p.N; pa.I = p.I; pa.bs = p.block_size; pa.Hkv = p.Hkv; pa.Tq = p.Tq; pa.CH = a.CH; pa.B = B;
-    pa.partial_mode = a.partial_mode; pa.W = W; pa.lens_given = lens_given ? 1 : 0; pa.max_blocks = max_blocks; pa.seq_lens = seq_lens;
-    pa.local_lens = local_lens; pa.ws = a.ws; pa.lay = lay; pa.U = a.U; pa.G = a.Gn;
-    pa.rows_per_group = a.rows; pa.Hq = p.Hq; pa.Dv = p.Dv; pa.out_partial = out_partial;
-    pa.lse_partial = lse_partial; pa.out = out; pa.lse = lse; pa.out_dtype = p.out_dtype;
-    launch_plan(pa, stream);
-    if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
-    count_launches(1);
+    if (mode != PlanMode::kPlanned) {
+        PlanArgs pa;
+        memset(&pa, 0, sizeof pa);
+        pa.N = p.N; pa.I = p.I; pa.bs = p.block_size; pa.Hkv = p.Hkv; pa.Tq = p.Tq; pa.CH = a.CH; pa.B = B;
+        pa.partial_mode = a.partial_mode; pa.W = W; pa.lens_given = lens_given ? 1 : 0; pa.max_blocks = max_blocks;
+        pa.worker_starts = a.worker_starts; pa.plan_key = a.plan_key; pa.seq_lens = seq_lens;
+        pa.local_lens = local_lens; pa.ws = a.ws; pa.lay = lay; pa.U = a.U; pa.G = a.Gn;
+        launch_plan(pa, stream);
+        if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
+        count_launches(1);
+        if (mode == PlanMode::kOnly) return DCP_OK;
+    }
 
     cudaError_t e = cudaSuccess;
     if (kern == Kernel::kGqaMma) {
@@ -461,6 +500,22 @@ int dcp_decode_attention(const dcp_params* params, int32_t B, const void* q, con
                          float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     return run_attention(params, B, q, k_pool, v_pool, num_blocks, block_tables, max_blocks, seq_lens,
                          local_lens, false, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream);
+}
+
+int dcp_decode_plan(const dcp_params* params, int32_t B, const int32_t* seq_lens, const int32_t* local_lens,
+                    int32_t max_blocks, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return run_attention(params, B, nullptr, nullptr, nullptr, 0, nullptr, max_blocks, seq_lens, local_lens, false,
+                         nullptr, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream, false,
+                         PlanMode::kOnly);
+}
+
+int dcp_decode_attention_planned(const dcp_params* params, int32_t B, const void* q, const void* k_pool,
+                                 const void* v_pool, int64_t num_blocks, const int32_t* block_tables,
+                                 int32_t max_blocks, const int32_t* seq_lens, const int32_t* local_lens, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return run_attention(params, B, q, k_pool, v_pool, num_blocks, block_tables, max_blocks, seq_lens, local_lens,
+                         false, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream, false,
+                         PlanMode::kPlanned);
 }
 
 int dcp_lse_merge(int32_t N, int64_t rows, int32_t Dv, const float* out_partial, const float* lse_partial,

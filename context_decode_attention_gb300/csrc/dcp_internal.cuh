@@ -61,8 +61,9 @@ __host__ __device__ __forceinline__ uint32_t local_len32(uint32_t L, int r, int 
 // ---------------------------------------------------------------------------
 struct WsHeader {
     uint32_t err;
-    uint32_t pad;
+    uint32_t n_empty;      // merge groups that own no chunk (listed at off_empty)
     int64_t total_chunks;
+    uint64_t plan_key;     // the arguments the plan was made for (plan_key_of)
     // block-transfer totals: per-block partials accumulate here, the last
     // block to finish publishes them and puts both words back to zero
     unsigned long long xfer_acc[2];
@@ -71,18 +72,28 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) <= 256, "the workspace header is 256 bytes");
 
 struct WsLayout {
-    size_t off_units, off_seg_base, off_counters, off_part_o, off_part_lse, off_qprep, total;
+    size_t off_units, off_seg_base, off_counters, off_wfirst, off_empty, off_part_o, off_part_lse, off_qprep, total;
 };
 
 __host__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// wfirst[w]: where worker w's chunk range starts (W workers), written by a
+// plan made ahead of its attention call, so that a worker starts with one
+// load instead of a search.  empty[i]: the merge groups that own no chunk.
+struct WorkerStart {
+    int64_t u0;              // the unit holding the worker's first chunk
+    int64_t ustart, uend;    // that unit's chunk range [unit_start[u0], unit_start[u0 + 1])
+    int64_t pad;
+};
 __host__ inline WsLayout ws_layout(int64_t U, int64_t G, int64_t seg_max, int64_t rows, int64_t Dv,
-                                   size_t qprep_bytes = 0) {
+                                   size_t qprep_bytes, int64_t W) {
     WsLayout l;
     size_t o = 256;
     l.off_units = o; o = align256(o + sizeof(int64_t) * (size_t)(U + 1));
     l.off_seg_base = o; o = align256(o + sizeof(int32_t) * (size_t)(G + 1));
     l.off_counters = o; o = align256(o + sizeof(uint32_t) * (size_t)(G + 1));
+    l.off_wfirst = o; o = align256(o + sizeof(WorkerStart) * (size_t)W);
+    l.off_empty = o; o = align256(o + sizeof(int32_t) * (size_t)G);
     l.off_part_o = o; o = align256(o + sizeof(float) * (size_t)seg_max * rows * Dv);
     l.off_part_lse = o; o = align256(o + sizeof(float) * (size_t)seg_max * rows);
     l.off_qprep = o; o = align256(o + qprep_bytes);
@@ -170,19 +181,13 @@ struct PlanArgs {
     int64_t W;         // workers of the attention kernel that follows
     int lens_given;    // local lengths are given, not derived (sparse staging)
     int max_blocks;
+    int worker_starts;    // also write each worker's first unit (a plan made ahead)
+    uint64_t plan_key;
     const int32_t* seq_lens;
     const int32_t* local_lens;
     uint8_t* ws;
     WsLayout lay;
     int64_t U, G;
-    // outputs for groups that own no chunk
-    int rows_per_group;   // Tq * (Hq / Hkv)
-    int Hq, Dv;
-    float* out_partial;   // partial mode
-    float* lse_partial;
-    void* out;            // decode mode
-    float* lse;
-    int out_dtype;
 };
 
 void launch_plan(const PlanArgs& a, cudaStream_t s);
@@ -207,6 +212,8 @@ struct AttnArgs {
     WsLayout lay;
     int rows;        // rows per group = Tq * G
     int lens_given;  // local lengths are given (sparse staging): they also bound each rank's tokens
+    int worker_starts;  // the plan holds each worker's first unit (wfirst)
+    uint64_t plan_key;  // must equal the workspace header's (a plan for other arguments: DCP_DEV_ERR_PLAN)
 };
 
 // Causal prefill of a PCP-partitioned chunk: per-rank partials of query rows
@@ -339,6 +346,34 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int d
         reinterpret_cast<float*>(out)[idx] = v;
     else
         reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+}
+
+// The output of a merge group that owns no chunk (the plan lists them): out
+// (or out_partial) zeros and lse -inf for its rows.  One warp.
+__device__ __forceinline__ void write_empty_group(const AttnArgs& a, int64_t g, int lane) {
+    int b, kvh, r = 0;
+    if (a.partial_mode) {
+        r = (int)(g % a.N);
+        b = (int)((g / a.N) / a.Hkv);
+        kvh = (int)((g / a.N) % a.Hkv);
+    } else {
+        b = (int)(g / a.Hkv);
+        kvh = (int)(g % a.Hkv);
+    }
+    const int64_t total = (int64_t)a.rows * a.Dv;
+    for (int64_t e = lane; e < total; e += 32) {
+        const int row = (int)(e / a.Dv), d = (int)(e % a.Dv);
+        const int t = row / a.G, gq = row % a.G;
+        const int64_t orow = ((int64_t)b * a.Tq + t) * a.Hq + (int64_t)kvh * a.G + gq;
+        if (a.partial_mode) {
+            const int64_t prow = (int64_t)r * a.B * a.Tq * a.Hq + orow;
+            a.out_partial[prow * a.Dv + d] = 0.f;
+            if (d == 0) a.lse_partial[prow] = -INFINITY;
+        } else {
+            store_out(a.out, orow * a.Dv + d, 0.f, a.out_dtype);
+            if (d == 0 && a.lse) a.lse[orow] = -INFINITY;
+        }
+    }
 }
 
 }  // namespace dcp

@@ -110,7 +110,7 @@ __global__ void segment_merge_kernel(AttnArgs a) {
     const float* part_lse = reinterpret_cast<const float*>(a.ws + a.lay.off_part_lse);
     const int base = seg_base[g];
     const int n = seg_base[g + 1] - base;
-    if (n == 0) return;  // the planner wrote this group's zeros / -inf
+    // n == 0: a group that owns no chunk; the merge below gives zeros and -inf
     int b, kvh, r = 0;
     if (a.partial_mode) {
         r = (int)(g % a.N);

@@ -47,7 +47,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     __shared__ int64_t warp_tot[32];
     __shared__ int64_t carry;
     __shared__ int64_t us_s[kUnitSmem + 1];
-    __shared__ int empty_list[kPlanThreads];
     __shared__ int n_empty;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
     int64_t* unit_start = reinterpret_cast<int64_t*>(a.ws + a.lay.off_units);
@@ -85,12 +84,31 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     __syncthreads();
     auto us_at = [&](int64_t i) -> int64_t { return i <= kUnitSmem ? us_s[i] : unit_start[i]; };
 
-    // 2. segments per merge group.  With fewer chunks than workers only the
-    // first P workers take part, so every worker in play owns >= 1 chunk.
-    // Groups that own no chunk (rare) get zeros and -inf.
+    // 2. each worker's first unit (the last u with unit_start[u] <= its first
+    // chunk) and that unit's chunk range.  Only a plan made ahead of its call
+    // does this: behind the planner the kernel's own search costs less than
+    // this pass does in the planner.
     const int64_t We = P < a.W ? P : a.W;
+    if (a.worker_starts) {
+        WorkerStart* wfirst = reinterpret_cast<WorkerStart*>(a.ws + a.lay.off_wfirst);
+        for (int64_t w = tid; w < We; w += kPlanThreads) {
+            const int64_t c0 = worker_begin(w, We, P);
+            int64_t lo = 0, hi = a.U - 1;
+            while (lo < hi) {
+                const int64_t mid = (lo + hi + 1) >> 1;
+                if (us_at(mid) <= c0) lo = mid; else hi = mid - 1;
+            }
+            wfirst[w] = WorkerStart{lo, us_at(lo), us_at(lo + 1), 0};
+        }
+    }
+
+    // 3. segments per merge group.  With fewer chunks than workers only the
+    // first P workers take part, so every worker in play owns >= 1 chunk.
+    // Groups that own no chunk (rare) are listed; the attention kernels give
+    // them zeros and -inf (the plan holds no output pointer, so one plan
+    // serves every call made with its arguments).
     const int64_t per_group = a.partial_mode ? 1 : a.N;
-    const int G = a.Hq / a.Hkv;
+    int32_t* empty = reinterpret_cast<int32_t*>(a.ws + a.lay.off_empty);
     for (int64_t base = 0; base < a.G; base += kPlanThreads) {
         const int64_t g = base + tid;
         int64_t cnt = 0;
@@ -98,44 +116,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             const int64_t first = us_at(g * per_group);
             const int64_t end = us_at((g + 1) * per_group);
             if (end > first) cnt = worker_of(end - 1, We, P) - worker_of(first, We, P) + 1;
-            else empty_list[atomicAdd(&n_empty, 1)] = (int)tid;
+            else empty[atomicAdd(&n_empty, 1)] = (int32_t)g;
             counters[g] = 0;
         }
         const int64_t incl = block_inclusive_scan(cnt, warp_tot);
         if (g < a.G) seg_base[g] = (int32_t)(carry + incl - cnt);
         __syncthreads();
         if (tid == kPlanThreads - 1) carry += incl;
-        for (int k = 0; k < n_empty; ++k) {
-            const int64_t gg = base + empty_list[k];
-            int b, kvh, r = 0;
-            if (a.partial_mode) {
-                r = (int)(gg % a.N);
-                b = (int)((gg / a.N) / a.Hkv);
-                kvh = (int)((gg / a.N) % a.Hkv);
-            } else {
-                b = (int)(gg / a.Hkv);
-                kvh = (int)(gg % a.Hkv);
-            }
-            const int64_t total = (int64_t)a.rows_per_group * a.Dv;
-            for (int64_t e = tid; e < total; e += kPlanThreads) {
-                const int row = (int)(e / a.Dv), d = (int)(e % a.Dv);
-                const int t = row / G, gq = row % G;
-                const int64_t orow = ((int64_t)b * a.Tq + t) * a.Hq + (int64_t)kvh * G + gq;
-                if (a.partial_mode) {
-                    const int64_t prow = (int64_t)r * a.B * a.Tq * a.Hq + orow;
-                    a.out_partial[prow * a.Dv + d] = 0.f;
-                    if (d == 0) a.lse_partial[prow] = -INFINITY;
-                } else {
-                    store_out(a.out, orow * a.Dv + d, 0.f, a.out_dtype);
-                    if (d == 0 && a.lse) a.lse[orow] = -INFINITY;
-                }
-            }
-        }
-        __syncthreads();
-        if (tid == 0) n_empty = 0;
         __syncthreads();
     }
-    if (tid == 0) seg_base[a.G] = (int32_t)carry;
+    if (tid == 0) {
+        seg_base[a.G] = (int32_t)carry;
+        hdr->n_empty = (uint32_t)n_empty;
+        hdr->plan_key = a.plan_key;
+    }
 }
 
 }  // namespace

@@ -13,7 +13,7 @@ import torch
 from dcp_workloads import allocate_blocks
 
 from . import (
-    dcp_decode_attention, dcp_get_error, dcp_lse_merge, dcp_partial_attention, dcp_pcp_partition,
+    dcp_decode_attention, dcp_decode_attention_planned, dcp_decode_plan, dcp_get_error, dcp_lse_merge, dcp_partial_attention, dcp_pcp_partition,
     dcp_prefill_attention, dcp_slot_mapping, dcp_workspace_init, dcp_workspace_size, params_from_config,
 )
 
@@ -113,10 +113,32 @@ class DeviceWorkload:
                              self.seq_lens, self.local_lens, self.out, self.lse, self.workspace, self.stream)
         return self.out, self.lse
 
-    def step(self):
-        """One decode step: cache write of the new tokens, then fused attention + merge."""
+    def plan_and_write(self):
+        """The step's work plan on a second stream while this one writes the new
+        tokens (the plan needs the lengths only); this stream waits for both."""
+        if getattr(self, "_pstream", None) is None:
+            self._pstream = torch.cuda.Stream(device=self.dev)
+            self._fork, self._join = torch.cuda.Event(), torch.cuda.Event()
+        self._fork.record(self.stream)
+        self._pstream.wait_event(self._fork)
+        dcp_decode_plan(self.params, self.seq_lens, self.local_lens, int(self.block_tables.shape[-1]),
+                        self.workspace, self._pstream)
+        self._join.record(self._pstream)
         self.write_new_tokens()
-        return self.decode()
+        self.stream.wait_event(self._join)
+
+    def decode_planned(self):
+        """Fused attention + merge on the plan plan_and_write made."""
+        dcp_decode_attention_planned(self.params, self.q, self.k_pool, self.v_pool, self.num_blocks,
+                                     self.block_tables, self.seq_lens, self.local_lens, self.out, self.lse,
+                                     self.workspace, self.stream)
+        return self.out, self.lse
+
+    def step(self):
+        """One decode step: the plan beside the cache write of the new tokens, then
+        fused attention + merge."""
+        self.plan_and_write()
+        return self.decode_planned()
 
     def partial(self):
         if self.out_partial is None:

@@ -81,6 +81,8 @@ extern "C" {
                                        kernel found its shared memory off the 1024-byte boundary
                                        its swizzled layouts need, and did nothing) */
 #define DCP_DEV_ERR_ROWS 0x20u      /* a request's padded prefill rows exceed the row capacity */
+#define DCP_DEV_ERR_PLAN 0x40u      /* dcp_decode_attention_planned found no plan in the workspace made
+                                       (by dcp_decode_plan) for its arguments, and did nothing */
 
 typedef enum { DCP_F32 = 0, DCP_BF16 = 1, DCP_FP8_E4M3 = 2 } dcp_dtype;
 typedef enum { DCP_LAYOUT_GQA = 0, DCP_LAYOUT_MLA = 1 } dcp_layout;
@@ -338,6 +340,40 @@ int dcp_decode_attention(const dcp_params* params, int32_t B, const void* q,
                          const int32_t* seq_lens, const int32_t* local_lens,
                          void* out, float* lse,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Decode attention in two calls: the work plan made ahead, then the attention.
+ *
+ * The plan (how the units of every (rank, request, KV head) are cut into
+ * chunks and dealt to the kernel's workers, and where each worker's segments
+ * merge; "vLLM DCP and PCP", Deep Dive 6, the partials and their merge)
+ * depends only on the lengths, not on the cache contents or the query.  A
+ * serving step knows the lengths before it writes the step's new tokens into
+ * the cache, so the plan can be made beside the cache write (another stream)
+ * or once per step for every layer, instead of in front of each attention.
+ *
+ * dcp_decode_plan writes the plan for (params, B, seq_lens, local_lens,
+ * max_blocks) into the workspace (dcp_workspace_size bytes); the device
+ * checks of dcp_decode_attention on the lengths run here.
+ * dcp_decode_attention_planned then computes exactly what
+ * dcp_decode_attention computes, with the same arguments, without planning.
+ * It must be ordered after the plan (same stream, or an event) and be made
+ * with the same params, B, max_blocks, workspace and the same seq_lens /
+ * local_lens pointers whose contents the plan saw.  One plan serves any number
+ * of such calls (each call leaves the plan as it found it), until another
+ * call on the same workspace writes a different plan (any dcp_decode_attention
+ * or dcp_partial_attention call does).  A call whose arguments differ from the
+ * plan's raises DCP_DEV_ERR_PLAN on the device and writes no output; a change
+ * of the lengths' contents under the same pointers is not detected.
+ */
+int dcp_decode_plan(const dcp_params* params, int32_t B, const int32_t* seq_lens, const int32_t* local_lens,
+                    int32_t max_blocks, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+int dcp_decode_attention_planned(const dcp_params* params, int32_t B, const void* q,
+                                 const void* k_pool, const void* v_pool, int64_t num_blocks,
+                                 const int32_t* block_tables, int32_t max_blocks,
+                                 const int32_t* seq_lens, const int32_t* local_lens,
+                                 void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Decode attention for callers that cannot allocate device memory.
