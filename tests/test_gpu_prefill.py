@@ -30,6 +30,13 @@ CASES = {
     "bs64_chunk192_k4": (config("gqa_llama8b", B=2, Tq=192, block_size=64, lengths=("list", [1000, 2600])), 4),
     "bs128_chunk100_k2_N3": (config("gqa_llama8b", B=2, Tq=100, block_size=128, N=3, I=2,
                                     lengths=("list", [100, 777])), 2),
+    # 64-token pages and the CTA's 128-row tiles: one row tile, an odd number of
+    # row tiles with G = 8, a last row tile that is mostly padding
+    "bs64_chunk24_k1_one_tile": (config("gqa_llama8b", B=2, Tq=24, block_size=64, lengths=("list", [500, 90])), 1),
+    "bs64_chunk72_k2_g8_odd_tiles": (config("gqa_llama8b", B=2, Tq=72, Hq=16, Hkv=2, block_size=64,
+                                            lengths=("list", [800, 300])), 2),
+    "bs64_chunk40_k3_part_pair": (config("gqa_llama8b", B=2, Tq=40, block_size=64, N=2, I=3,
+                                         lengths=("list", [1000, 77])), 3),
 }
 
 _cache = {}
