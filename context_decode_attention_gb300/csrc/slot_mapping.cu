@@ -39,6 +39,44 @@ __device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, int 
     }
 }
 
+// The token's rows of every KV head (K, then V) from their contiguous copy in
+// new_k / new_v to their slots in the pools, 16-byte pieces only: every lane
+// loads all of its pieces of a batch before it stores any, so a batch costs
+// one memory round trip (a load-store pair per head costs one per head).
+__device__ __forceinline__ void scatter_token16(const SlotArgs& a, int64_t t, int64_t blk, int64_t off, int lane) {
+    const int krow = a.Dk * a.kv_esize, vrow = a.Dv * a.kv_esize;
+    const int kq = krow / 16, vq = vrow / 16;  // 16-byte pieces per row
+    const int nk = a.Hkv * kq, n = nk + (a.new_v ? a.Hkv * vq : 0);
+    const uint4* ks = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.new_k) + t * a.Hkv * krow);
+    const uint4* vs = a.new_v ? reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.new_v) + t * a.Hkv * vrow)
+                              : nullptr;
+    auto dst_of = [&](int i) -> uint4* {
+        if (i < nk) {
+            const int h = i / kq;
+            return reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.k_pool) + ((blk * a.Hkv + h) * a.bs + off) * krow) +
+                   (i - h * kq);
+        }
+        i -= nk;
+        const int h = i / vq;
+        return reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.v_pool) + ((blk * a.Hkv + h) * a.bs + off) * vrow) +
+               (i - h * vq);
+    };
+    constexpr int kBatch = 8;
+    for (int base = 0; base < n; base += 32 * kBatch) {
+        uint4 v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = base + lane + 32 * j;
+            if (i < n) v[j] = i < nk ? ks[i] : vs[i - nk];
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = base + lane + 32 * j;
+            if (i < n) *dst_of(i) = v[j];
+        }
+    }
+}
+
 // One warp per token: ownership, local position, slot, and the row copy.
 __global__ void token_kernel(SlotArgs a) {
     const int lane = threadIdx.x & 31;
@@ -76,6 +114,13 @@ __global__ void token_kernel(SlotArgs a) {
         for (int r = lane; r < a.N; r += 32) a.slots[(int64_t)r * a.T + t] = (r == owner) ? slot : -1;
     if (slot < 0 || a.new_k == nullptr) return;
     const int64_t blk = slot / a.bs, off = slot % a.bs;
+    const int krow16 = a.Dk * a.kv_esize, vrow16 = a.Dv * a.kv_esize;
+    if (((reinterpret_cast<uintptr_t>(a.new_k) | reinterpret_cast<uintptr_t>(a.new_v) |
+          reinterpret_cast<uintptr_t>(a.k_pool) | reinterpret_cast<uintptr_t>(a.v_pool) | (uintptr_t)krow16 |
+          (uintptr_t)(a.new_v ? vrow16 : 0)) & 15u) == 0) {
+        scatter_token16(a, t, blk, off, lane);  // MLA: one head (Hkv 1), no V rows
+        return;
+    }
     if (a.layout == DCP_LAYOUT_MLA) {
         const int row = a.Dk * a.kv_esize;
         warp_copy(reinterpret_cast<uint8_t*>(a.k_pool) + (blk * a.bs + off) * row,
