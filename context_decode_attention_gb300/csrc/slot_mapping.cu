@@ -40,40 +40,53 @@ __device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, int 
 }
 
 // The token's rows of every KV head (K, then V) from their contiguous copy in
-// new_k / new_v to their slots in the pools, 16-byte pieces only: every lane
-// loads all of its pieces of a batch before it stores any, so a batch costs
-// one memory round trip (a load-store pair per head costs one per head).
-__device__ __forceinline__ void scatter_token16(const SlotArgs& a, int64_t t, int64_t blk, int64_t off, int lane) {
+// new_k / new_v to their slots in the pools, 16-byte pieces only.  The pieces
+// of one batch (32 lanes x kBatch) are loaded before the slot is known, so the
+// row loads overlap the ownership / block-table lookups, and stored after.
+constexpr int kBatch = 8;
+struct TokenRows {
+    int kq, vq, nk, n;  // 16-byte pieces per K row, per V row; K pieces; all pieces
+    const uint4* ks;
+    const uint4* vs;
+};
+__device__ __forceinline__ TokenRows token_rows(const SlotArgs& a, int64_t t) {
+    TokenRows r;
     const int krow = a.Dk * a.kv_esize, vrow = a.Dv * a.kv_esize;
-    const int kq = krow / 16, vq = vrow / 16;  // 16-byte pieces per row
-    const int nk = a.Hkv * kq, n = nk + (a.new_v ? a.Hkv * vq : 0);
-    const uint4* ks = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.new_k) + t * a.Hkv * krow);
-    const uint4* vs = a.new_v ? reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.new_v) + t * a.Hkv * vrow)
-                              : nullptr;
-    auto dst_of = [&](int i) -> uint4* {
-        if (i < nk) {
-            const int h = i / kq;
-            return reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.k_pool) + ((blk * a.Hkv + h) * a.bs + off) * krow) +
-                   (i - h * kq);
-        }
-        i -= nk;
-        const int h = i / vq;
-        return reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.v_pool) + ((blk * a.Hkv + h) * a.bs + off) * vrow) +
-               (i - h * vq);
-    };
-    constexpr int kBatch = 8;
-    for (int base = 0; base < n; base += 32 * kBatch) {
-        uint4 v[kBatch];
+    r.kq = krow / 16;
+    r.vq = vrow / 16;
+    r.nk = a.Hkv * r.kq;
+    r.n = r.nk + (a.new_v ? a.Hkv * r.vq : 0);
+    r.ks = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.new_k) + t * a.Hkv * krow);
+    r.vs = a.new_v ? reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.new_v) + t * a.Hkv * vrow)
+                   : nullptr;
+    return r;
+}
+__device__ __forceinline__ void load_batch(const TokenRows& r, int base, int lane, uint4 (&v)[kBatch]) {
 #pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            const int i = base + lane + 32 * j;
-            if (i < n) v[j] = i < nk ? ks[i] : vs[i - nk];
-        }
+    for (int j = 0; j < kBatch; ++j) {
+        const int i = base + lane + 32 * j;
+        if (i < r.n) v[j] = i < r.nk ? r.ks[i] : r.vs[i - r.nk];
+    }
+}
+__device__ __forceinline__ void store_batch(const SlotArgs& a, const TokenRows& r, int64_t blk, int64_t off, int base,
+                                            int lane, const uint4 (&v)[kBatch]) {
+    const int krow = r.kq * 16, vrow = r.vq * 16;
 #pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            const int i = base + lane + 32 * j;
-            if (i < n) *dst_of(i) = v[j];
+    for (int j = 0; j < kBatch; ++j) {
+        int i = base + lane + 32 * j;
+        if (i >= r.n) continue;
+        uint4* dst;
+        if (i < r.nk) {
+            const int h = i / r.kq;
+            dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.k_pool) + ((blk * a.Hkv + h) * a.bs + off) * krow) +
+                  (i - h * r.kq);
+        } else {
+            i -= r.nk;
+            const int h = i / r.vq;
+            dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.v_pool) + ((blk * a.Hkv + h) * a.bs + off) * vrow) +
+                  (i - h * r.vq);
         }
+        *dst = v[j];
     }
 }
 
@@ -82,24 +95,40 @@ __global__ void token_kernel(SlotArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t t = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     if (t >= a.T) return;
+    // 16-byte pieces when every end allows them (MLA: one head, no V rows)
+    const bool v16 = a.new_k != nullptr &&
+                     ((reinterpret_cast<uintptr_t>(a.new_k) | reinterpret_cast<uintptr_t>(a.new_v) |
+                       reinterpret_cast<uintptr_t>(a.k_pool) | reinterpret_cast<uintptr_t>(a.v_pool) |
+                       (uintptr_t)(a.Dk * a.kv_esize) | (uintptr_t)(a.new_v ? a.Dv * a.kv_esize : 0)) & 15u) == 0;
+    TokenRows rows{};
+    uint4 first[kBatch];
+    if (v16) {
+        rows = token_rows(a, t);
+        load_batch(rows, 0, lane, first);  // in flight during the lookups below
+    }
     int owner = -1;
     int64_t slot = -1;
     int b = 0;
     if (lane == 0) {
         b = a.tok_req[t];
         const int64_t pos = a.tok_pos[t];
-        if (b < 0 || b >= a.B || pos < 0 || pos >= (int64_t)a.seq_lens[b]) {
+        if (b < 0 || b >= a.B || pos < 0) {
             raise_err(a.err, DCP_DEV_ERR_TOKEN);
         } else {
-            owner = (int)owner_rank(pos, a.N, a.I);
-            if (a.block_tables) {
-                const int64_t lp = local_pos(pos, a.N, a.I);
-                const int64_t blk_idx = lp / a.bs;
-                if (blk_idx >= a.max_blocks) {
-                    raise_err(a.err, DCP_DEV_ERR_TABLE);
-                } else {
-                    const int32_t id = a.block_tables[((int64_t)owner * a.B + b) * a.max_blocks + blk_idx];
-                    if (id < 0 || id >= a.num_blocks)
+            // the block-table read goes out beside the length check
+            const int own = (int)owner_rank(pos, a.N, a.I);
+            const int64_t lp = local_pos(pos, a.N, a.I);
+            const int64_t blk_idx = lp / a.bs;
+            const bool in_table = a.block_tables && blk_idx < a.max_blocks;
+            const int32_t id = in_table ? a.block_tables[((int64_t)own * a.B + b) * a.max_blocks + blk_idx] : -1;
+            if (pos >= (int64_t)a.seq_lens[b]) {
+                raise_err(a.err, DCP_DEV_ERR_TOKEN);
+            } else {
+                owner = own;
+                if (a.block_tables) {
+                    if (!in_table)
+                        raise_err(a.err, DCP_DEV_ERR_TABLE);
+                    else if (id < 0 || id >= a.num_blocks)
                         raise_err(a.err, DCP_DEV_ERR_BLOCK_ID);
                     else
                         slot = (int64_t)id * a.bs + lp % a.bs;
@@ -114,11 +143,13 @@ __global__ void token_kernel(SlotArgs a) {
         for (int r = lane; r < a.N; r += 32) a.slots[(int64_t)r * a.T + t] = (r == owner) ? slot : -1;
     if (slot < 0 || a.new_k == nullptr) return;
     const int64_t blk = slot / a.bs, off = slot % a.bs;
-    const int krow16 = a.Dk * a.kv_esize, vrow16 = a.Dv * a.kv_esize;
-    if (((reinterpret_cast<uintptr_t>(a.new_k) | reinterpret_cast<uintptr_t>(a.new_v) |
-          reinterpret_cast<uintptr_t>(a.k_pool) | reinterpret_cast<uintptr_t>(a.v_pool) | (uintptr_t)krow16 |
-          (uintptr_t)(a.new_v ? vrow16 : 0)) & 15u) == 0) {
-        scatter_token16(a, t, blk, off, lane);  // MLA: one head (Hkv 1), no V rows
+    if (v16) {
+        store_batch(a, rows, blk, off, 0, lane, first);
+        for (int base = 32 * kBatch; base < rows.n; base += 32 * kBatch) {
+            uint4 v[kBatch];
+            load_batch(rows, base, lane, v);
+            store_batch(a, rows, blk, off, base, lane, v);
+        }
         return;
     }
     if (a.layout == DCP_LAYOUT_MLA) {
