@@ -105,6 +105,37 @@ def test_null_pointers_and_workspace_rejected(libdcp):
     assert rc == 1
 
 
+def test_plan_ahead_entry_points_validate_before_launching(libdcp):
+    """dcp_decode_plan and dcp_decode_attention_planned refuse bad arguments on
+    the host, before any device query or launch (codes: 1 invalid argument, 4
+    workspace), and an empty batch is a no-op."""
+    p = _good()
+    dummy = ctypes.c_void_p(256)
+    # the plan: lengths and a block-table width are all it needs
+    assert libdcp.dcp_decode_plan(ctypes.byref(p), 0, None, None, 4, None, 0, None) == 0
+    assert libdcp.dcp_decode_plan(ctypes.byref(p), -1, dummy, dummy, 4, dummy, 1 << 20, None) == 1
+    assert libdcp.dcp_decode_plan(ctypes.byref(p), 4, None, dummy, 4, dummy, 1 << 20, None) == 1
+    assert libdcp.dcp_decode_plan(ctypes.byref(p), 4, dummy, None, 4, dummy, 1 << 20, None) == 1
+    assert libdcp.dcp_decode_plan(ctypes.byref(p), 4, dummy, dummy, 0, dummy, 1 << 20, None) == 1
+    assert libdcp.dcp_decode_plan(ctypes.byref(p), 4, dummy, dummy, 4, None, 1 << 20, None) == 4
+    bad = _good()
+    bad.N = 0
+    assert libdcp.dcp_decode_plan(ctypes.byref(bad), 4, dummy, dummy, 4, dummy, 1 << 20, None) == 1
+    # the planned attention: the fused call's argument rules
+    f = libdcp.dcp_decode_attention_planned
+    assert f(ctypes.byref(p), 0, None, None, None, 0, None, 4, None, None, None, None, None, 0, None) == 0
+    assert f(ctypes.byref(p), 4, None, dummy, dummy, 10, dummy, 4, dummy, dummy, dummy, None, dummy, 1 << 20,
+             None) == 1
+    assert f(ctypes.byref(p), 4, dummy, dummy, None, 10, dummy, 4, dummy, dummy, dummy, None, dummy, 1 << 20,
+             None) == 1  # a GQA call needs the value pool
+    assert f(ctypes.byref(p), 4, dummy, dummy, dummy, 10, dummy, 4, dummy, dummy, None, None, dummy, 1 << 20,
+             None) == 1  # no output
+    assert f(ctypes.byref(p), 4, dummy, dummy, dummy, 10, dummy, 4, dummy, dummy, dummy, None, None, 0,
+             None) == 4  # no workspace
+    assert f(ctypes.byref(p), 4, dummy, ctypes.c_void_p(258), dummy, 10, dummy, 4, dummy, dummy, dummy, None,
+             dummy, 1 << 20, None) == 1  # misaligned pool
+
+
 def test_slot_mapping_argument_rules(libdcp):
     p = _good()
     dummy = ctypes.c_void_p(256)
