@@ -52,8 +52,8 @@ MEASURED_TRAFFIC = {
                              (219.794688e6 + 4.131584e6) / 376734),
     ("mla_tcgen05", "bf16"): ("attn_mla_pair.cu", "6ac87a4a8535bfa083190d7c2022c347b6d9b360423382eb90936f588f2a8cb3",
                               (308.545280e6 + 5.903872e6) / 262144),
-    ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "9d31b23c14236492fd2c9524cfc867eccb94955c4798f3dbe5f577c081e66e5f",
-                          (268.683008e6 + 3.034112e6) / 65536),
+    ("gqa_mma", "bf16"): ("attn_gqa_mma.cu", "67755412d54aa3ba8046b17584b4ccddeaf57333dc06d2d86f49ad71f0006772",
+                          (268.675840e6 + 2.791168e6) / 65536),
     # per table entry (N B max_blocks) of the block-transfer listing
     ("transfer_blocks", "entry"): ("transfer.cu", "ba69fc5af5bf509387a4668d62e0fd322f75cc04daf9e1105750d478aee93893",
                                    (161.792e3 + 0.0) / (8 * 16 * 284)),

@@ -13,7 +13,10 @@
 //    KV head = 2 x 16 x D bf16, contiguous inside one physical block) of all
 //    units are dealt to workers as equal contiguous ranges;
 //  * each warp keeps NST chunks in flight with 16-byte cp.async.cg copies into
-//    an XOR-swizzled smem ring (conflict-free ldmatrix);
+//    an XOR-swizzled smem ring (conflict-free ldmatrix), under an L2
+//    evict-first policy: the pages are read once, and streaming them through
+//    L2 at the default priority evicted the plan, block tables and partials
+//    that the kernel reads again (6 us of a 32 x 8K-token step);
 //  * S = Q K^T and O += P V on mma.sync.m16n8k16 (bf16 in, fp32 accumulate),
 //    online softmax in base 2 on the accumulator fragments;
 //  * a segment's result is either final (the group lies in one worker) or a
@@ -105,6 +108,8 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
     };
     ld_unit();
 
+    uint64_t l2_first;  // the pages are read once: L2 evicts them first
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(l2_first));
     // ---- producer: issue the copies of chunk cc into its ring stage
     auto issue = [&](int64_t cc) {
         if (cc < c1) {
@@ -125,8 +130,10 @@ __global__ void __launch_bounds__(kWarps * 32) gqa_mma_kernel(AttnArgs a) {
                 for (int i = lane; i < C::kPieces; i += 32) {
                     const int row = i / (D / 8), pc = i % (D / 8);
                     const uint32_t so = row * C::kRowBytes + ((pc ^ (row & 7)) << 4);
-                    cp_async16(st + so, ks + i * 16);
-                    cp_async16(st + C::kTileBytes + so, vs + i * 16);
+                    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;\n" ::"r"(st + so),
+                                 "l"(ks + i * 16), "l"(l2_first) : "memory");
+                    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;\n" ::"r"(st + C::kTileBytes + so),
+                                 "l"(vs + i * 16), "l"(l2_first) : "memory");
                 }
             }
         }
