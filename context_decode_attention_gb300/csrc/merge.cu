@@ -165,6 +165,19 @@ __global__ void lse_merge_kernel(int N, int64_t rows, int Dv, const float* o_par
     if (row >= rows) return;
     auto o = [&](int i, int d) { return o_parts[((int64_t)i * rows + row) * Dv + d]; };
     auto l = [&](int i) { return lse_parts[(int64_t)i * rows + row]; };
+    // rows of a multiple of 128 columns at 16-byte aligned addresses: the vector
+    // merge (weights once per part, independent 16-byte loads)
+    const uintptr_t ends = reinterpret_cast<uintptr_t>(o_parts) | reinterpret_cast<uintptr_t>(out);
+    if (Dv % 128 == 0 && (ends & 15u) == 0) {
+        auto o4 = [&](int i, int k) {
+            return *reinterpret_cast<const float4*>(o_parts + ((int64_t)i * rows + row) * Dv + 128 * k + 4 * lane);
+        };
+        const float L = warp_merge_row_v4(
+            N, Dv, o4, l, [&](int k, float4 v) { store_out4(out, row * Dv + 128 * k + 4 * lane, v, out_dtype); },
+            lane);
+        if (lane == 0 && lse) lse[row] = L;
+        return;
+    }
     const float L = warp_merge_row(
         N, Dv, o, l, [&](int d, float v) { store_out(out, row * Dv + d, v, out_dtype); }, lane);
     if (lane == 0 && lse) lse[row] = L;
