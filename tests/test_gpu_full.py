@@ -93,7 +93,7 @@ def test_full_size_prefill():
 
 
 def test_full_size_sparse():
-    """The sparse workload (config 4's contexts, 4 query tokens per request,
+    """The sparse workload (the 16 mixed-context MLA requests, 4 query tokens per request,
     2,048 candidates per token) exactly as the bench runs it: localisation
     bit-exact for every row, merged output of sampled query tokens (all heads)
     against the oracle's attention over their candidates."""
